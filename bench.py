@@ -1,0 +1,425 @@
+"""Benchmark of the per-unit FSDP cycle on GB300.
+
+One step = one fsdp_step (gather, gather again under reshard-after-forward,
+reduce-scatter, AdamW) on every unit of the workload, N virtual ranks per
+unit.  Default workload: two minGPT-175B transformer blocks (d=12288,
+ffn=49152; 1,812,099,072 parameters per block, one FlatParameter each), N=8
+virtual ranks, bf16 per-rank gradients reduced in fp32, fp32 master weights
+and Adam state.  Inputs are synthetic (seeded) and far larger than L2, so no
+L2 flush is needed between steps.
+
+Metric: counted HBM bytes per step / step time (GB/s).  Counted bytes per
+unit step, every required read and write once:
+    gather      R x (4P read fp32 master + 2P write bf16)          R = 2
+    reduce-sc.  N*g_b*P read (N gradients) + 4P write (fp32 shards)
+    AdamW       16P read (p, g, m, v) + 12P write (p, m, v) + 2P (bf16 shadow)
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME] [--e2e-steps E] [--no-e2e] [--no-cpu-baseline]
+With --gpus N > 1 (under torchrun) every rank runs an independent replica of
+the workload on its own GPU (the N virtual ranks of a unit never span GPUs);
+value = all ranks' counted bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from fully_sharded_unit_gb300 import workloads  # noqa: E402
+
+METRIC = "FSDP unit-step HBM GB/s (gather+reduce-scatter+AdamW) and % of GB300 HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------- helpers
+
+def counted_bytes(wl: workloads.Workload, unit: int) -> dict:
+    P, N = wl.unit_numel(unit), wl.N
+    gb = 4 if wl.grad_dtype == "f32" else 2
+    R = 2 if wl.reshard_after_forward else 1
+    return dict(gather=6 * P, reduce_scatter=(N * gb + 4) * P, adamw=30 * P,
+                step=R * 6 * P + (N * gb + 4) * P + 30 * P, gathers=R,
+                h2d=N * gb * P, d2h=2 * P)
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    with open(os.path.join(ROOT, "fully_sharded_unit_gb300", "csrc", "kernels.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary line
+    `kernel workload bytes_per_launch kernels_cu_sha`; None when absent or
+    when the kernel source has changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_source_sha()
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 4 and not line.startswith("#") and f[0] == kernel and f[1] == workload and f[3] == sha:
+            return int(float(f[2]))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device: int):
+        self.proc = None
+        self.device = device
+
+    def __enter__(self):
+        smi = shutil.which("nvidia-smi")
+        if smi is None:
+            return self
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.device).uuid)
+            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            ident = str(self.device)
+        self.proc = subprocess.Popen([smi, "-i", ident, f"--query-gpu={','.join(self.FIELDS)}",
+                                      "--format=csv,noheader,nounits", "-lms", "200"],
+                                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.result = None
+        if self.proc is None:
+            return False
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if sm:
+            self.result = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                           "reasons": sorted(reasons), "samples": len(sm)}
+        return False
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def dist_max(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample_workload(wl: workloads.Workload, S: int) -> workloads.Workload:
+    """A bounded sample of the workload: one FLAT unit of S elements with the
+    same N, gradient dtype, distributions and hyper-parameters."""
+    largest = max(wl.units[0], key=lambda p: workloads.Workload.unit_numel(
+        wl.with_(units=((p,),)), 0))
+    unit = (workloads.Param("sample", (S,), largest.init),)
+    return wl.with_(name=wl.name + f"_sample{S}", units=(unit,), layout="flat")
+
+
+def time_oracle_steps(wl: workloads.Workload, target_s: float, n_steps: int):
+    """Oracle step times on a sample sized for about target_s per step.
+    Returns (list of per-step seconds, sample elements, counted bytes per step)."""
+    import numpy as np
+    from oracle import fsdp_oracle as O
+
+    def one(sw, orc, grads):
+        t0 = time.perf_counter()
+        orc.step(grads)
+        return time.perf_counter() - t0
+
+    def make(S):
+        sw = oracle_sample_workload(wl, S)
+        params = [p.numpy() for p in workloads.param_tensors(sw, 0)]
+        grads = []
+        for r in range(sw.N):
+            g = workloads.grad_tensor(sw, 0, 0, r)
+            grads.append(g.numpy() if g.dtype == torch.float32 else g.view(torch.int16).numpy().view(np.uint16))
+        orc = O.UnitOracle(sw.shapes(0), sw.N, "flat", O.AdamWHyper(**workloads.hyper(sw)),
+                           sw.reshard_after_forward)
+        orc.load(params)
+        return sw, orc, grads
+
+    S = 1 << 20
+    sw, orc, grads = make(S)
+    dt = one(sw, orc, grads)
+    S = int(min(1 << 26, max(1 << 20, S * target_s / max(dt, 1e-6))))
+    sw, orc, grads = make(S)
+    times = [one(sw, orc, grads) for _ in range(n_steps)]
+    return times, S, counted_bytes(sw, 0)["step"]
+
+
+def cpu_cores_info():
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except Exception:
+        aff = os.cpu_count()
+    return aff
+
+
+# --------------------------------------------------------------------------- arms
+
+def run_reference(args, world, rank):
+    """The oracle as it stands, on the host cores: each step is one oracle unit
+    step on a bounded sample of the workload."""
+    if rank != 0:
+        return
+    wl = workloads.get(args.workload)
+    times, S, cb = time_oracle_steps(wl, target_s=args.ref_step_seconds, n_steps=args.warmup + args.steps)
+    timed = times[args.warmup:]
+    sec = sum(timed)
+    value = cb * len(timed) / sec / 1e9
+    cpu = {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": f"one FLAT unit of {S} elements drawn like {wl.name} (N={wl.N}, {wl.grad_dtype} grads), "
+                     f"one oracle step per bench step", "host_cores_available": cpu_cores_info()}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(timed),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": wl.name, "sample_elements": S},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    from fully_sharded_unit_gb300 import binding as B
+    from fully_sharded_unit_gb300.build import build
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build()
+    B.lib()
+    wl = workloads.get(args.workload)
+    hp = workloads.hyper(wl)
+    units = []
+    for i in range(wl.n_units):
+        u = B.Unit(wl.shapes(i), wl.layout, wl.N, wl.grad_dtype, wl.reshard_after_forward)
+        params = workloads.param_tensors(wl, i, dev)
+        u.load(params)
+        torch.cuda.synchronize()
+        del params
+        units.append(u)
+    P_max = max(u.numel for u in units)
+    # the N ranks' full gradients (one backward's output), reused by every unit
+    grads = [torch.empty(P_max, dtype=wl.torch_grad_dtype(), device=dev) for _ in range(wl.N)]
+    for r in range(wl.N):
+        workloads.grad_tensor(wl, 0, 0, r, dev, out=grads[r][:units[0].numel])
+    out = torch.empty(P_max, dtype=torch.int16, device=dev)
+    cb = [counted_bytes(wl, i) for i in range(wl.n_units)]
+    step_bytes = sum(c["step"] for c in cb)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for i, u in enumerate(units):
+            g = grads if units[i].numel == P_max else [x[:u.numel] for x in grads]
+            u.step(g, out, hp, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for u in units:
+        B.fsdp_profile_reset(u.handle)
+        B.fsdp_profile_enable(u.handle, True)
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    dist_barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    for u in units:
+        B.fsdp_profile_enable(u.handle, False)
+    ms_max = dist_max(ms, world, dev)
+
+    # per-kernel device time over the timed region (events on the launch stream)
+    per_kernel = {}
+    launches = 0
+    for k in ("gather", "reduce_scatter", "adamw"):
+        tot, n = 0.0, 0
+        for u in units:
+            t, c = B.fsdp_profile_read(u.handle, k)
+            tot, n = tot + t, n + c
+        per_kernel[k] = (tot, n)
+        launches += n
+    dom = max(per_kernel, key=lambda k: per_kernel[k][0])
+    dom_ms, dom_n = per_kernel[dom]
+    dom_bytes = sum(c[dom] * (c["gathers"] if dom == "gather" else 1) for c in cb) / \
+        (dom_n / args.steps)      # counted bytes per launch
+    achieved = dom_bytes / (dom_ms / dom_n * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": peak_kind,
+                "traffic": recorded_traffic(dom, wl.name),
+                "per_kernel_ms_per_launch": {k: (v[0] / v[1] if v[1] else None) for k, v in per_kernel.items()},
+                "per_kernel_gbs": {k: (sum(c[k] * (c["gathers"] if k == "gather" else 1) for c in cb) /
+                                       (v[1] / args.steps) / (v[0] / v[1] * 1e-3) / 1e9 if v[1] else None)
+                                   for k, v in per_kernel.items()}}
+
+    value_rank = step_bytes * args.steps / (ms * 1e-3) / 1e9
+    value = world * step_bytes * args.steps / (ms_max * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world)
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        times, S, ccb = time_oracle_steps(wl, target_s=args.cpu_seconds / 3, n_steps=3)
+        cpu = {"value": ccb * len(times) / sum(times) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"3 oracle unit steps on one FLAT unit of {S} elements drawn like {wl.name} "
+                         f"(N={wl.N}, {wl.grad_dtype} grads)", "host_cores_available": cpu_cores_info()}
+
+    for u in units:
+        u.close()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "pct_of_hbm_peak": 100.0 * value_rank / peak, "hbm_peak_gbs": peak, "hbm_peak_source": peak_kind,
+        "config": {"workload": wl.name, "units": wl.n_units, "params_per_unit": [u_ for u_ in
+                   (wl.unit_numel(i) for i in range(wl.n_units))], "virtual_ranks": wl.N,
+                   "layout": wl.layout, "grad_dtype": wl.grad_dtype,
+                   "reshard_after_forward": wl.reshard_after_forward,
+                   "counted_bytes_per_step": step_bytes, "gather_source": "fp32 master",
+                   "l2": "inputs larger than L2; no flush", "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clk.result,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world):
+    """Same metric through the public API with the gradients in pinned host
+    memory: every step copies each unit's N gradients host->device, runs
+    fsdp_step, and copies the gathered bf16 parameters device->host."""
+    P_max = grads[0].numel()
+    host_grads = [torch.empty(P_max, dtype=grads[0].dtype, pin_memory=True) for _ in grads]
+    for h, g in zip(host_grads, grads):
+        h.copy_(g)
+    host_out = torch.empty(P_max, dtype=torch.int16, pin_memory=True)
+
+    def step():
+        for u in units:
+            for h, g in zip(host_grads, grads):
+                g[:u.numel].copy_(h[:u.numel], non_blocking=True)
+            u.step([g[:u.numel] for g in grads], out, hp, stream)
+            host_out[:u.numel].copy_(out[:u.numel], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    ms = dist_max(ev0.elapsed_time(ev1), world, dev)
+    h2d = sum(c["h2d"] for c in cb)
+    d2h = sum(c["d2h"] for c in cb)
+    del host_grads, host_out
+    return {"value": world * step_bytes * args.e2e_steps / (ms * 1e-3) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+            "ms_per_step": ms / args.e2e_steps}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mingpt175b_flat", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if world != args.gpus and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,377 @@
+"""ctypes binding of the C ABI in ``include/fsdp_unit.h``.
+
+Argument marshalling only: every function here has the C name, turns torch
+tensors and Python values into pointers and sizes, checks that buffers are
+large enough (the C side cannot see sizes), calls the library and raises
+``FsdpError`` on a non-zero status.  No step of the per-unit cycle runs in
+Python.  The library is loaded from the package's ``_lib`` directory; if it
+is missing, every call raises (there is no fallback).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+import torch
+
+from .build import LIB
+
+# ---- constants (mirror include/fsdp_unit.h) ------------------------------
+FSDP_OK = 0
+FSDP_E_INVALID_ARG = -1
+FSDP_E_OOM = -2
+FSDP_E_CUDA = -3
+FSDP_E_STATE = -4
+FSDP_E_ALIGN = -5
+FSDP_E_CAPACITY = -6
+
+FSDP_LAYOUT_FLAT = 0
+FSDP_LAYOUT_DIM0 = 1
+FSDP_DTYPE_F32 = 0
+FSDP_DTYPE_BF16 = 1
+
+FSDP_STATE_PARAM = 0
+FSDP_STATE_GRAD = 1
+FSDP_STATE_EXP_AVG = 2
+FSDP_STATE_EXP_AVG_SQ = 3
+FSDP_STATE_SHADOW = 4
+
+FSDP_KERNEL_SHARD_IN = 0
+FSDP_KERNEL_GATHER = 1
+FSDP_KERNEL_REDUCE_SCATTER = 2
+FSDP_KERNEL_ADAMW = 3
+FSDP_KERNEL_COUNT = 4
+
+LAYOUTS = {"flat": FSDP_LAYOUT_FLAT, "dim0": FSDP_LAYOUT_DIM0}
+GRAD_DTYPES = {"f32": FSDP_DTYPE_F32, "bf16": FSDP_DTYPE_BF16}
+STATES = {"param": FSDP_STATE_PARAM, "grad": FSDP_STATE_GRAD, "exp_avg": FSDP_STATE_EXP_AVG,
+          "exp_avg_sq": FSDP_STATE_EXP_AVG_SQ, "shadow": FSDP_STATE_SHADOW}
+KERNELS = {"shard_in": FSDP_KERNEL_SHARD_IN, "gather": FSDP_KERNEL_GATHER,
+           "reduce_scatter": FSDP_KERNEL_REDUCE_SCATTER, "adamw": FSDP_KERNEL_ADAMW}
+
+
+class Segment(ctypes.Structure):
+    _fields_ = [("rank", ctypes.c_int32), ("param", ctypes.c_int32), ("global_off", ctypes.c_int64),
+                ("shard_off", ctypes.c_int64), ("arena_off", ctypes.c_int64), ("len", ctypes.c_int64)]
+
+
+class AdamWHp(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double)]
+
+
+class UnitConfig(ctypes.Structure):
+    _fields_ = [("layout", ctypes.c_int), ("num_ranks", ctypes.c_int), ("grad_dtype", ctypes.c_int),
+                ("reshard_after_forward", ctypes.c_int)]
+
+
+class FsdpError(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str):
+        super().__init__(f"{where}: {detail} (code {code})")
+        self.code = code
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_PI64 = ctypes.POINTER(ctypes.c_int64)
+_PI = ctypes.POINTER(ctypes.c_int)
+
+_SIGNATURES = {
+    "fsdp_plan_layout": (_I, [_I, _PI, _PI64, _I, _I, _PI64, _PI64, ctypes.POINTER(Segment), _I64]),
+    "fsdp_unit_create": (_I, [_I, _PI, _PI64, ctypes.POINTER(UnitConfig), ctypes.POINTER(_P)]),
+    "fsdp_unit_destroy": (_I, [_P]),
+    "fsdp_load_params": (_I, [_P, ctypes.POINTER(_P), _P]),
+    "fsdp_allgather": (_I, [_P, _P, _P]),
+    "fsdp_reduce_scatter": (_I, [_P, ctypes.POINTER(_P), _P]),
+    "fsdp_adamw_step": (_I, [_P, ctypes.POINTER(AdamWHp), _P]),
+    "fsdp_step": (_I, [_P, ctypes.POINTER(_P), _P, ctypes.POINTER(AdamWHp), _P]),
+    "fsdp_get_state": (_I, [_P, _I, _I, _P, _P]),
+    "fsdp_set_state": (_I, [_P, _I, _I, _P, _P]),
+    "fsdp_read_global": (_I, [_P, _I, _I64, _I64, _P, _P]),
+    "fsdp_get_step_count": (_I, [_P, _PI64]),
+    "fsdp_set_step_count": (_I, [_P, _I64]),
+    "fsdp_unit_info": (_I, [_P, _PI64, _PI, _PI, _PI, _PI]),
+    "fsdp_unit_segments": (_I, [_P, ctypes.POINTER(Segment), _I64, _PI64]),
+    "fsdp_memory_report": (_I, [_P, _I, _PI64, _PI64, _PI64, _PI64, _PI64]),
+    "fsdp_profile_enable": (_I, [_P, _I]),
+    "fsdp_profile_read": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), _PI64]),
+    "fsdp_profile_reset": (_I, [_P]),
+    "fsdp_strerror": (ctypes.c_char_p, [_I]),
+    "fsdp_last_error": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library.  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(
+                f"CUDA library {LIB} is not built; run fully_sharded_unit_gb300.build.build() "
+                "(there is no CPU fallback)")
+        l = ctypes.CDLL(LIB)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != FSDP_OK:
+        detail = lib().fsdp_last_error().decode() or lib().fsdp_strerror(rc).decode()
+        raise FsdpError(rc, where, detail)
+
+
+def _shape_args(shapes: Sequence[Sequence[int]]):
+    nd = (ctypes.c_int * len(shapes))(*[len(s) for s in shapes])
+    flat = [int(d) for s in shapes for d in s]
+    dims = (ctypes.c_int64 * max(1, len(flat)))(*flat)
+    return len(shapes), nd, dims
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _hp(hp) -> AdamWHp:
+    if isinstance(hp, AdamWHp):
+        return hp
+    return AdamWHp(float(hp["lr"]), float(hp["beta1"]), float(hp["beta2"]), float(hp["eps"]),
+                   float(hp["weight_decay"]))
+
+
+def _ptrs(tensors) -> ctypes.Array:
+    return (_P * len(tensors))(*[t.data_ptr() if t is not None else None for t in tensors])
+
+
+# ---- C entry points -----------------------------------------------------
+
+def fsdp_plan_layout(shapes, layout, num_ranks):
+    """(P, [Segment, ...]) for a unit; host only."""
+    n, nd, dims = _shape_args(shapes)
+    P = ctypes.c_int64()
+    ns = ctypes.c_int64()
+    _check(lib().fsdp_plan_layout(n, nd, dims, LAYOUTS.get(layout, layout), num_ranks,
+                                  ctypes.byref(P), ctypes.byref(ns), None, 0), "fsdp_plan_layout")
+    segs = (Segment * max(1, ns.value))()
+    _check(lib().fsdp_plan_layout(n, nd, dims, LAYOUTS.get(layout, layout), num_ranks,
+                                  ctypes.byref(P), ctypes.byref(ns), segs, ns.value), "fsdp_plan_layout")
+    return P.value, list(segs)[:ns.value]
+
+
+def fsdp_unit_create(shapes, layout, num_ranks, grad_dtype="f32", reshard_after_forward=True):
+    n, nd, dims = _shape_args(shapes)
+    cfg = UnitConfig(LAYOUTS.get(layout, layout), int(num_ranks), GRAD_DTYPES.get(grad_dtype, grad_dtype),
+                     1 if reshard_after_forward else 0)
+    h = _P()
+    _check(lib().fsdp_unit_create(n, nd, dims, ctypes.byref(cfg), ctypes.byref(h)), "fsdp_unit_create")
+    return h
+
+
+def fsdp_unit_destroy(h) -> None:
+    _check(lib().fsdp_unit_destroy(h), "fsdp_unit_destroy")
+
+
+def fsdp_unit_info(h):
+    P = ctypes.c_int64()
+    N, lay, gd, raf = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().fsdp_unit_info(h, ctypes.byref(P), ctypes.byref(N), ctypes.byref(lay), ctypes.byref(gd),
+                                ctypes.byref(raf)), "fsdp_unit_info")
+    return dict(numel=P.value, num_ranks=N.value, layout=lay.value, grad_dtype=gd.value,
+                reshard_after_forward=bool(raf.value))
+
+
+def fsdp_unit_segments(h):
+    ns = ctypes.c_int64()
+    _check(lib().fsdp_unit_segments(h, None, 0, ctypes.byref(ns)), "fsdp_unit_segments")
+    segs = (Segment * max(1, ns.value))()
+    _check(lib().fsdp_unit_segments(h, segs, ns.value, ctypes.byref(ns)), "fsdp_unit_segments")
+    return list(segs)[:ns.value]
+
+
+def fsdp_load_params(h, params, stream=None) -> None:
+    for p in params:
+        assert p.dtype == torch.float32 and p.is_contiguous() and (p.numel() == 0 or p.is_cuda)
+    _check(lib().fsdp_load_params(h, _ptrs(params), _stream(stream)), "fsdp_load_params")
+
+
+def fsdp_allgather(h, out: torch.Tensor, stream=None) -> None:
+    P = fsdp_unit_info(h)["numel"]
+    assert out.is_cuda and out.element_size() == 2 and out.is_contiguous() and out.numel() >= P
+    _check(lib().fsdp_allgather(h, out.data_ptr(), _stream(stream)), "fsdp_allgather")
+
+
+def _check_grads(h, grads):
+    info = fsdp_unit_info(h)
+    assert len(grads) == info["num_ranks"]
+    want = torch.float32 if info["grad_dtype"] == FSDP_DTYPE_F32 else torch.bfloat16
+    for g in grads:
+        assert g.is_cuda and g.is_contiguous() and g.numel() >= info["numel"]
+        assert g.dtype == want, f"gradient dtype {g.dtype}, unit expects {want}"
+
+
+def fsdp_reduce_scatter(h, grads, stream=None) -> None:
+    _check_grads(h, grads)
+    _check(lib().fsdp_reduce_scatter(h, _ptrs(grads), _stream(stream)), "fsdp_reduce_scatter")
+
+
+def fsdp_adamw_step(h, hp, stream=None) -> None:
+    hp = _hp(hp)
+    _check(lib().fsdp_adamw_step(h, ctypes.byref(hp), _stream(stream)), "fsdp_adamw_step")
+
+
+def fsdp_step(h, grads, out: torch.Tensor, hp, stream=None) -> None:
+    _check_grads(h, grads)
+    P = fsdp_unit_info(h)["numel"]
+    assert out.is_cuda and out.element_size() == 2 and out.is_contiguous() and out.numel() >= P
+    hp = _hp(hp)
+    _check(lib().fsdp_step(h, _ptrs(grads), out.data_ptr(), ctypes.byref(hp), _stream(stream)),
+           "fsdp_step")
+
+
+def _shard_len(h, rank):
+    return sum(s.len for s in fsdp_unit_segments(h) if s.rank == rank)
+
+
+def fsdp_get_state(h, which, rank, dst: torch.Tensor, stream=None) -> None:
+    which = STATES.get(which, which)
+    assert dst.is_contiguous() and dst.element_size() == (2 if which == FSDP_STATE_SHADOW else 4)
+    assert dst.numel() >= _shard_len(h, rank)
+    _check(lib().fsdp_get_state(h, which, rank, dst.data_ptr(), _stream(stream)), "fsdp_get_state")
+
+
+def fsdp_set_state(h, which, rank, src: torch.Tensor, stream=None) -> None:
+    which = STATES.get(which, which)
+    assert src.is_contiguous() and src.element_size() == (2 if which == FSDP_STATE_SHADOW else 4)
+    assert src.numel() >= _shard_len(h, rank)
+    _check(lib().fsdp_set_state(h, which, rank, src.data_ptr(), _stream(stream)), "fsdp_set_state")
+
+
+def fsdp_read_global(h, which, begin, count, dst: torch.Tensor, stream=None) -> None:
+    which = STATES.get(which, which)
+    assert dst.is_contiguous() and dst.element_size() == (2 if which == FSDP_STATE_SHADOW else 4)
+    assert dst.numel() >= count
+    _check(lib().fsdp_read_global(h, which, int(begin), int(count), dst.data_ptr(), _stream(stream)),
+           "fsdp_read_global")
+
+
+def fsdp_get_step_count(h) -> int:
+    t = ctypes.c_int64()
+    _check(lib().fsdp_get_step_count(h, ctypes.byref(t)), "fsdp_get_step_count")
+    return t.value
+
+
+def fsdp_set_step_count(h, t: int) -> None:
+    _check(lib().fsdp_set_step_count(h, int(t)), "fsdp_set_step_count")
+
+
+def fsdp_memory_report(h, rank):
+    vals = [ctypes.c_int64() for _ in range(5)]
+    _check(lib().fsdp_memory_report(h, rank, *[ctypes.byref(v) for v in vals]), "fsdp_memory_report")
+    return dict(zip(("param", "grad", "adam", "shadow", "pad"), (v.value for v in vals)))
+
+
+def fsdp_profile_enable(h, on=True) -> None:
+    _check(lib().fsdp_profile_enable(h, 1 if on else 0), "fsdp_profile_enable")
+
+
+def fsdp_profile_read(h, kernel):
+    ms = ctypes.c_double()
+    n = ctypes.c_int64()
+    _check(lib().fsdp_profile_read(h, KERNELS.get(kernel, kernel), ctypes.byref(ms), ctypes.byref(n)),
+           "fsdp_profile_read")
+    return ms.value, n.value
+
+
+def fsdp_profile_reset(h) -> None:
+    _check(lib().fsdp_profile_reset(h), "fsdp_profile_reset")
+
+
+def fsdp_strerror(code: int) -> str:
+    return lib().fsdp_strerror(code).decode()
+
+
+def fsdp_last_error() -> str:
+    return lib().fsdp_last_error().decode()
+
+
+# ---- a small owning wrapper ----------------------------------------------
+
+class Unit:
+    """Owns one ``fsdp_unit`` handle; methods call the C entry points."""
+
+    def __init__(self, shapes, layout="flat", num_ranks=1, grad_dtype="f32", reshard_after_forward=True):
+        self.shapes = [tuple(int(d) for d in s) for s in shapes]
+        self.handle = fsdp_unit_create(self.shapes, layout, num_ranks, grad_dtype, reshard_after_forward)
+        info = fsdp_unit_info(self.handle)
+        self.numel = info["numel"]
+        self.N = info["num_ranks"]
+        self.grad_dtype = grad_dtype
+        self.segments = fsdp_unit_segments(self.handle)
+        self.shard_len = [0] * self.N
+        for s in self.segments:
+            self.shard_len[s.rank] += s.len
+
+    def close(self):
+        if self.handle is not None:
+            fsdp_unit_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def load(self, params, stream=None):
+        fsdp_load_params(self.handle, params, stream)
+
+    def allgather(self, out, stream=None):
+        fsdp_allgather(self.handle, out, stream)
+
+    def reduce_scatter(self, grads, stream=None):
+        fsdp_reduce_scatter(self.handle, grads, stream)
+
+    def adamw_step(self, hp, stream=None):
+        fsdp_adamw_step(self.handle, hp, stream)
+
+    def step(self, grads, out, hp, stream=None):
+        fsdp_step(self.handle, grads, out, hp, stream)
+
+    def get_state(self, which, rank, device="cuda"):
+        dt = torch.int16 if STATES.get(which, which) == FSDP_STATE_SHADOW else torch.float32
+        dst = torch.empty(self.shard_len[rank], dtype=dt, device=device)
+        if dst.numel():
+            fsdp_get_state(self.handle, which, rank, dst)
+        return dst
+
+    def set_state(self, which, rank, src, stream=None):
+        fsdp_set_state(self.handle, which, rank, src, stream)
+
+    def read_global(self, which, begin=0, count=None, device="cuda"):
+        count = self.numel - begin if count is None else count
+        dt = torch.int16 if STATES.get(which, which) == FSDP_STATE_SHADOW else torch.float32
+        dst = torch.empty(count, dtype=dt, device=device)
+        fsdp_read_global(self.handle, which, begin, count, dst)
+        return dst
+
+    @property
+    def step_count(self):
+        return fsdp_get_step_count(self.handle)
+
+    @step_count.setter
+    def step_count(self, t):
+        fsdp_set_step_count(self.handle, t)
+
+    def memory_report(self, rank):
+        return fsdp_memory_report(self.handle, rank)

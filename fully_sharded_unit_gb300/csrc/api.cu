@@ -1,0 +1,557 @@
+// C ABI of the per-unit FSDP cycle (declared in include/fsdp_unit.h).
+//
+// A unit owns five slabs of length plan.slab_len (fp32 master, fp32 gradient
+// shard, fp32 m, fp32 v, bf16 shadow); rank k's arena is
+// [arena_base[k], arena_base[k] + arena_len[k]) of each.  Pads are zero from
+// creation and stay zero: the gather and reduce-scatter never touch them and
+// AdamW maps (p, g, m, v) = 0 to 0.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "fsdp_unit.h"
+#include "kernels.hpp"
+#include "plan.hpp"
+
+using fsdp::Plan;
+using fsdp::Tile;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& why) {
+    g_last_error = why;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(FSDP_E_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct ProfRecord {
+    int kind;
+    cudaEvent_t start;
+    cudaEvent_t stop;
+};
+
+class DeviceGuard {
+public:
+    explicit DeviceGuard(int device) : device_(device) {
+        if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
+        if (prev_ != device_) ok_ = cudaSetDevice(device_) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        if (prev_ >= 0 && prev_ != device_) cudaSetDevice(prev_);
+    }
+    bool ok() const { return ok_; }
+
+private:
+    int device_;
+    int prev_ = -1;
+    bool ok_ = true;
+};
+
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+}  // namespace
+
+struct fsdp_unit {
+    int device = 0;
+    Plan plan;
+    int nparams = 0;
+    int grad_dtype = FSDP_DTYPE_F32;
+    int raf = 1;
+    float* master = nullptr;
+    float* grad = nullptr;
+    float* m = nullptr;
+    float* v = nullptr;
+    uint16_t* shadow = nullptr;
+    Tile* tiles = nullptr;
+    int64_t ntiles = 0;
+    Tile* load_tiles = nullptr;
+    int64_t nload_tiles = 0;
+    fsdp::ParamSrc* param_src = nullptr;
+    fsdp::KernelGrids grids{};
+    int64_t t = 0;
+    bool loaded = false;
+    bool profiling = false;
+    std::vector<ProfRecord> prof;
+};
+
+namespace {
+
+void free_unit(fsdp_unit* u) {
+    for (void* p : {static_cast<void*>(u->master), static_cast<void*>(u->grad),
+                    static_cast<void*>(u->m), static_cast<void*>(u->v),
+                    static_cast<void*>(u->shadow), static_cast<void*>(u->tiles),
+                    static_cast<void*>(u->load_tiles), static_cast<void*>(u->param_src)}) {
+        if (p) cudaFree(p);
+    }
+    for (auto& r : u->prof) {
+        cudaEventDestroy(r.start);
+        cudaEventDestroy(r.stop);
+    }
+    u->prof.clear();
+}
+
+// Launch `fn` bracketed by profiler events when profiling is on.
+template <typename F>
+int profiled_launch(fsdp_unit* u, int kind, cudaStream_t st, const char* what, F&& fn) {
+    ProfRecord rec{kind, nullptr, nullptr};
+    if (u->profiling) {
+        if (cudaEventCreate(&rec.start) != cudaSuccess || cudaEventCreate(&rec.stop) != cudaSuccess)
+            return fail(FSDP_E_CUDA, "cudaEventCreate failed");
+        cudaEventRecord(rec.start, st);
+    }
+    cudaError_t e = fn();
+    if (e != cudaSuccess) {
+        if (rec.start) cudaEventDestroy(rec.start);
+        if (rec.stop) cudaEventDestroy(rec.stop);
+        return cuda_fail(e, what);
+    }
+    if (u->profiling) {
+        cudaEventRecord(rec.stop, st);
+        u->prof.push_back(rec);
+    }
+    return FSDP_OK;
+}
+
+float* state_f32(const fsdp_unit* u, int which) {
+    switch (which) {
+        case FSDP_STATE_PARAM: return u->master;
+        case FSDP_STATE_GRAD: return u->grad;
+        case FSDP_STATE_EXP_AVG: return u->m;
+        case FSDP_STATE_EXP_AVG_SQ: return u->v;
+        default: return nullptr;
+    }
+}
+
+// base pointer and element size of a state, or nullptr for a bad `which`
+char* state_base(const fsdp_unit* u, int which, size_t* esz) {
+    if (which == FSDP_STATE_SHADOW) {
+        *esz = 2;
+        return reinterpret_cast<char*>(u->shadow);
+    }
+    *esz = 4;
+    return reinterpret_cast<char*>(state_f32(u, which));
+}
+
+int check_unit(const fsdp_unit* u, bool need_loaded) {
+    if (u == nullptr) return fail(FSDP_E_INVALID_ARG, "unit is null");
+    if (need_loaded && !u->loaded) return fail(FSDP_E_STATE, "fsdp_load_params has not been called");
+    return FSDP_OK;
+}
+
+int check_hp(const fsdp_adamw_hp* hp) {
+    if (hp == nullptr) return fail(FSDP_E_INVALID_ARG, "hp is null");
+    auto fin = [](double x) { return std::isfinite(x); };
+    if (!fin(hp->lr) || !fin(hp->beta1) || !fin(hp->beta2) || !fin(hp->eps) || !fin(hp->weight_decay))
+        return fail(FSDP_E_INVALID_ARG, "AdamW hyper-parameters must be finite");
+    if (hp->lr < 0 || hp->eps < 0 || hp->weight_decay < 0)
+        return fail(FSDP_E_INVALID_ARG, "lr, eps and weight_decay must be >= 0");
+    if (!(hp->beta1 >= 0 && hp->beta1 < 1) || !(hp->beta2 >= 0 && hp->beta2 < 1))
+        return fail(FSDP_E_INVALID_ARG, "betas must be in [0, 1)");
+    return FSDP_OK;
+}
+
+int check_grads(const fsdp_unit* u, const void* const* grads) {
+    if (grads == nullptr) return fail(FSDP_E_INVALID_ARG, "grads array is null");
+    for (int r = 0; r < u->plan.N; ++r) {
+        if (grads[r] == nullptr) return fail(FSDP_E_INVALID_ARG, "a gradient pointer is null");
+        if (!aligned32(grads[r])) return fail(FSDP_E_ALIGN, "a gradient buffer is not 32-byte aligned");
+    }
+    return FSDP_OK;
+}
+
+int check_out(const uint16_t* out) {
+    if (out == nullptr) return fail(FSDP_E_INVALID_ARG, "output buffer is null");
+    if (!aligned32(out)) return fail(FSDP_E_ALIGN, "output buffer is not 32-byte aligned");
+    return FSDP_OK;
+}
+
+fsdp::AdamWConsts adamw_consts(const fsdp_adamw_hp* hp, int64_t t) {
+    const double bc1 = 1.0 - std::pow(hp->beta1, static_cast<double>(t));
+    const double bc2 = 1.0 - std::pow(hp->beta2, static_cast<double>(t));
+    fsdp::AdamWConsts c;
+    c.decay = static_cast<float>(1.0 - hp->lr * hp->weight_decay);
+    c.b1 = static_cast<float>(hp->beta1);
+    c.c1 = static_cast<float>(1.0 - hp->beta1);
+    c.b2 = static_cast<float>(hp->beta2);
+    c.c2 = static_cast<float>(1.0 - hp->beta2);
+    c.bc2 = static_cast<float>(bc2);
+    c.step = static_cast<float>(hp->lr / bc1);
+    c.eps = static_cast<float>(hp->eps);
+    return c;
+}
+
+int enqueue_gather(fsdp_unit* u, uint16_t* out, cudaStream_t st) {
+    return profiled_launch(u, FSDP_KERNEL_GATHER, st, "gather launch", [&] {
+        return fsdp::launch_gather(u->tiles, u->ntiles, u->master, out, u->grids.gather, st);
+    });
+}
+
+int enqueue_reduce_scatter(fsdp_unit* u, const void* const* grads, cudaStream_t st) {
+    return profiled_launch(u, FSDP_KERNEL_REDUCE_SCATTER, st, "reduce-scatter launch", [&] {
+        return fsdp::launch_reduce_scatter(u->tiles, u->ntiles, grads, u->plan.N, u->grad_dtype,
+                                           u->grad, u->grids.reduce_small, u->grids.reduce_large, st);
+    });
+}
+
+int enqueue_adamw(fsdp_unit* u, const fsdp_adamw_hp* hp, cudaStream_t st) {
+    const fsdp::AdamWConsts c = adamw_consts(hp, u->t + 1);
+    int rc = profiled_launch(u, FSDP_KERNEL_ADAMW, st, "AdamW launch", [&] {
+        return fsdp::launch_adamw(u->plan.slab_len / 8, u->master, u->grad, u->m, u->v, u->shadow, c,
+                                  u->grids.adamw, st);
+    });
+    if (rc == FSDP_OK) u->t += 1;
+    return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fsdp_strerror(int code) {
+    switch (code) {
+        case FSDP_OK: return "ok";
+        case FSDP_E_INVALID_ARG: return "invalid argument";
+        case FSDP_E_OOM: return "out of memory";
+        case FSDP_E_CUDA: return "CUDA error";
+        case FSDP_E_STATE: return "invalid state";
+        case FSDP_E_ALIGN: return "misaligned buffer";
+        case FSDP_E_CAPACITY: return "output array too small";
+        default: return "unknown error";
+    }
+}
+
+const char* fsdp_last_error(void) { return g_last_error.c_str(); }
+
+int fsdp_plan_layout(int nparams, const int* ndims, const int64_t* dims, int layout, int num_ranks,
+                     int64_t* numel, int64_t* nsegs, fsdp_segment* segs, int64_t cap) {
+    Plan plan;
+    std::string err;
+    int rc = fsdp::build_plan(nparams, ndims, dims, layout, num_ranks, &plan, &err);
+    if (rc != FSDP_OK) return fail(rc, err);
+    const int64_t n = static_cast<int64_t>(plan.segs.size());
+    if (numel) *numel = plan.P;
+    if (nsegs) *nsegs = n;
+    if (segs) {
+        if (cap < n) return fail(FSDP_E_CAPACITY, "segment array too small");
+        std::memcpy(segs, plan.segs.data(), sizeof(fsdp_segment) * static_cast<size_t>(n));
+    }
+    return FSDP_OK;
+}
+
+int fsdp_unit_create(int nparams, const int* ndims, const int64_t* dims,
+                     const fsdp_unit_config* cfg, fsdp_unit** out) {
+    if (out == nullptr || cfg == nullptr) return fail(FSDP_E_INVALID_ARG, "cfg/out is null");
+    *out = nullptr;
+    if (cfg->grad_dtype != FSDP_DTYPE_F32 && cfg->grad_dtype != FSDP_DTYPE_BF16)
+        return fail(FSDP_E_INVALID_ARG, "grad_dtype must be FSDP_DTYPE_F32 or FSDP_DTYPE_BF16");
+    Plan plan;
+    std::string err;
+    int rc = fsdp::build_plan(nparams, ndims, dims, cfg->layout, cfg->num_ranks, &plan, &err);
+    if (rc != FSDP_OK) return fail(rc, err);
+
+    fsdp_unit* u = new (std::nothrow) fsdp_unit;
+    if (u == nullptr) return fail(FSDP_E_OOM, "host allocation failed");
+    if (cudaGetDevice(&u->device) != cudaSuccess) {
+        delete u;
+        return fail(FSDP_E_CUDA, "no CUDA device");
+    }
+    u->plan = std::move(plan);
+    u->nparams = nparams;
+    u->grad_dtype = cfg->grad_dtype;
+    u->raf = cfg->reshard_after_forward ? 1 : 0;
+
+    std::vector<Tile> tiles, load_tiles;
+    fsdp::build_tiles(u->plan, &tiles);
+    fsdp::build_load_tiles(u->plan, &load_tiles);
+    u->ntiles = static_cast<int64_t>(tiles.size());
+    u->nload_tiles = static_cast<int64_t>(load_tiles.size());
+
+    const size_t S = static_cast<size_t>(u->plan.slab_len);
+    struct Alloc {
+        void** p;
+        size_t bytes;
+    } allocs[] = {
+        {reinterpret_cast<void**>(&u->master), S * 4},
+        {reinterpret_cast<void**>(&u->grad), S * 4},
+        {reinterpret_cast<void**>(&u->m), S * 4},
+        {reinterpret_cast<void**>(&u->v), S * 4},
+        {reinterpret_cast<void**>(&u->shadow), S * 2},
+        {reinterpret_cast<void**>(&u->tiles), tiles.size() * sizeof(Tile)},
+        {reinterpret_cast<void**>(&u->load_tiles), load_tiles.size() * sizeof(Tile)},
+        {reinterpret_cast<void**>(&u->param_src), static_cast<size_t>(nparams) * sizeof(fsdp::ParamSrc)},
+    };
+    for (auto& a : allocs) {
+        cudaError_t e = cudaMalloc(a.p, a.bytes > 0 ? a.bytes : 32);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            free_unit(u);
+            delete u;
+            return fail(e == cudaErrorMemoryAllocation ? FSDP_E_OOM : FSDP_E_CUDA,
+                        std::string("cudaMalloc: ") + cudaGetErrorString(e));
+        }
+    }
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < 5 && e == cudaSuccess; ++i) e = cudaMemset(*allocs[i].p, 0, allocs[i].bytes);
+    if (e == cudaSuccess && !tiles.empty())
+        e = cudaMemcpy(u->tiles, tiles.data(), tiles.size() * sizeof(Tile), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !load_tiles.empty())
+        e = cudaMemcpy(u->load_tiles, load_tiles.data(), load_tiles.size() * sizeof(Tile),
+                       cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = fsdp::query_grids(u->device, u->grad_dtype, &u->grids);
+    if (e != cudaSuccess) {
+        free_unit(u);
+        delete u;
+        return cuda_fail(e, "unit set-up");
+    }
+    *out = u;
+    return FSDP_OK;
+}
+
+int fsdp_unit_destroy(fsdp_unit* u) {
+    if (u == nullptr) return FSDP_OK;
+    DeviceGuard dg(u->device);
+    cudaDeviceSynchronize();
+    free_unit(u);
+    delete u;
+    return FSDP_OK;
+}
+
+int fsdp_load_params(fsdp_unit* u, const float* const* params, void* stream) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    if (params == nullptr) return fail(FSDP_E_INVALID_ARG, "params array is null");
+    std::vector<fsdp::ParamSrc> src(u->nparams);
+    for (int p = 0; p < u->nparams; ++p) {
+        const fsdp::ParamInfo& pi = u->plan.params[p];
+        if (pi.numel > 0 && params[p] == nullptr)
+            return fail(FSDP_E_INVALID_ARG, "a parameter pointer is null");
+        if ((reinterpret_cast<uintptr_t>(params[p]) & 3u) != 0)
+            return fail(FSDP_E_ALIGN, "a parameter buffer is not 4-byte aligned");
+        src[p] = fsdp::ParamSrc{params[p], pi.offset};
+    }
+    DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t S = static_cast<size_t>(u->plan.slab_len);
+    cudaError_t e = cudaMemcpyAsync(u->param_src, src.data(), src.size() * sizeof(fsdp::ParamSrc),
+                                    cudaMemcpyHostToDevice, st);
+    // pageable source: the copy has been staged when cudaMemcpyAsync returns
+    if (e == cudaSuccess) e = cudaMemsetAsync(u->master, 0, S * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(u->grad, 0, S * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(u->m, 0, S * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(u->v, 0, S * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(u->shadow, 0, S * 2, st);
+    if (e != cudaSuccess) return cuda_fail(e, "load set-up");
+    rc = profiled_launch(u, FSDP_KERNEL_SHARD_IN, st, "shard-in launch", [&] {
+        return fsdp::launch_shard_in(u->load_tiles, u->nload_tiles, u->param_src, u->master, u->shadow,
+                                     u->grids.shard_in, st);
+    });
+    if (rc) return rc;
+    u->t = 0;
+    u->loaded = true;
+    return FSDP_OK;
+}
+
+int fsdp_allgather(fsdp_unit* u, uint16_t* out, void* stream) {
+    int rc = check_unit(u, true);
+    if (rc == FSDP_OK) rc = check_out(out);
+    if (rc) return rc;
+    DeviceGuard dg(u->device);
+    return enqueue_gather(u, out, static_cast<cudaStream_t>(stream));
+}
+
+int fsdp_reduce_scatter(fsdp_unit* u, const void* const* grads, void* stream) {
+    int rc = check_unit(u, true);
+    if (rc == FSDP_OK) rc = check_grads(u, grads);
+    if (rc) return rc;
+    DeviceGuard dg(u->device);
+    return enqueue_reduce_scatter(u, grads, static_cast<cudaStream_t>(stream));
+}
+
+int fsdp_adamw_step(fsdp_unit* u, const fsdp_adamw_hp* hp, void* stream) {
+    int rc = check_unit(u, true);
+    if (rc == FSDP_OK) rc = check_hp(hp);
+    if (rc) return rc;
+    DeviceGuard dg(u->device);
+    return enqueue_adamw(u, hp, static_cast<cudaStream_t>(stream));
+}
+
+int fsdp_step(fsdp_unit* u, const void* const* grads, uint16_t* out, const fsdp_adamw_hp* hp,
+              void* stream) {
+    int rc = check_unit(u, true);
+    if (rc == FSDP_OK) rc = check_out(out);
+    if (rc == FSDP_OK) rc = check_grads(u, grads);
+    if (rc == FSDP_OK) rc = check_hp(hp);
+    if (rc) return rc;
+    DeviceGuard dg(u->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = enqueue_gather(u, out, st);                       // forward
+    if (rc == FSDP_OK && u->raf) rc = enqueue_gather(u, out, st);   // backward re-gather
+    if (rc == FSDP_OK) rc = enqueue_reduce_scatter(u, grads, st);
+    if (rc == FSDP_OK) rc = enqueue_adamw(u, hp, st);
+    return rc;
+}
+
+static int copy_state(const fsdp_unit* u, int which, int rank, void* ext, bool to_unit, void* stream) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    if (rank < 0 || rank >= u->plan.N) return fail(FSDP_E_INVALID_ARG, "rank out of range");
+    size_t esz = 0;
+    char* base = state_base(u, which, &esz);
+    if (base == nullptr) return fail(FSDP_E_INVALID_ARG, "unknown state");
+    if (ext == nullptr && u->plan.shard_len[rank] > 0) return fail(FSDP_E_INVALID_ARG, "buffer is null");
+    DeviceGuard dg(u->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t abase = u->plan.arena_base[rank];
+    for (int64_t i = u->plan.rank_first_seg[rank]; i < u->plan.rank_first_seg[rank + 1]; ++i) {
+        const fsdp_segment& s = u->plan.segs[i];
+        char* dev = base + static_cast<size_t>(abase + s.arena_off) * esz;
+        char* host = static_cast<char*>(ext) + static_cast<size_t>(s.shard_off) * esz;
+        cudaError_t e = to_unit ? cudaMemcpyAsync(dev, host, s.len * esz, cudaMemcpyDefault, st)
+                                : cudaMemcpyAsync(host, dev, s.len * esz, cudaMemcpyDefault, st);
+        if (e != cudaSuccess) return cuda_fail(e, "state copy");
+    }
+    return FSDP_OK;
+}
+
+int fsdp_get_state(const fsdp_unit* u, int which, int rank, void* dst, void* stream) {
+    return copy_state(u, which, rank, dst, false, stream);
+}
+
+int fsdp_set_state(fsdp_unit* u, int which, int rank, const void* src, void* stream) {
+    return copy_state(u, which, rank, const_cast<void*>(src), true, stream);
+}
+
+int fsdp_read_global(const fsdp_unit* u, int which, int64_t begin, int64_t count, void* dst,
+                     void* stream) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    if (begin < 0 || count < 0 || begin + count > u->plan.P)
+        return fail(FSDP_E_INVALID_ARG, "range outside the unit");
+    size_t esz = 0;
+    char* base = state_base(u, which, &esz);
+    if (base == nullptr) return fail(FSDP_E_INVALID_ARG, "unknown state");
+    if (count > 0 && dst == nullptr) return fail(FSDP_E_INVALID_ARG, "dst is null");
+    DeviceGuard dg(u->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t end = begin + count;
+    for (const fsdp_segment& s : u->plan.segs) {
+        const int64_t a = s.global_off > begin ? s.global_off : begin;
+        const int64_t b = s.global_off + s.len < end ? s.global_off + s.len : end;
+        if (b <= a) continue;
+        const int64_t slab = u->plan.arena_base[s.rank] + s.arena_off + (a - s.global_off);
+        cudaError_t e = cudaMemcpyAsync(static_cast<char*>(dst) + static_cast<size_t>(a - begin) * esz,
+                                        base + static_cast<size_t>(slab) * esz,
+                                        static_cast<size_t>(b - a) * esz, cudaMemcpyDefault, st);
+        if (e != cudaSuccess) return cuda_fail(e, "state copy");
+    }
+    return FSDP_OK;
+}
+
+int fsdp_get_step_count(const fsdp_unit* u, int64_t* t) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    if (t == nullptr) return fail(FSDP_E_INVALID_ARG, "t is null");
+    *t = u->t;
+    return FSDP_OK;
+}
+
+int fsdp_set_step_count(fsdp_unit* u, int64_t t) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    if (t < 0) return fail(FSDP_E_INVALID_ARG, "step count must be >= 0");
+    u->t = t;
+    return FSDP_OK;
+}
+
+int fsdp_unit_info(const fsdp_unit* u, int64_t* numel, int* num_ranks, int* layout, int* grad_dtype,
+                   int* raf) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    if (numel) *numel = u->plan.P;
+    if (num_ranks) *num_ranks = u->plan.N;
+    if (layout) *layout = u->plan.layout;
+    if (grad_dtype) *grad_dtype = u->grad_dtype;
+    if (raf) *raf = u->raf;
+    return FSDP_OK;
+}
+
+int fsdp_unit_segments(const fsdp_unit* u, fsdp_segment* segs, int64_t cap, int64_t* nsegs) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    const int64_t n = static_cast<int64_t>(u->plan.segs.size());
+    if (nsegs) *nsegs = n;
+    if (segs) {
+        if (cap < n) return fail(FSDP_E_CAPACITY, "segment array too small");
+        std::memcpy(segs, u->plan.segs.data(), sizeof(fsdp_segment) * static_cast<size_t>(n));
+    }
+    return FSDP_OK;
+}
+
+int fsdp_memory_report(const fsdp_unit* u, int rank, int64_t* param_bytes, int64_t* grad_bytes,
+                       int64_t* adam_bytes, int64_t* shadow_bytes, int64_t* pad_bytes) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    if (rank < 0 || rank >= u->plan.N) return fail(FSDP_E_INVALID_ARG, "rank out of range");
+    const int64_t n = u->plan.shard_len[rank];
+    const int64_t pads = u->plan.arena_len[rank] - n;
+    if (param_bytes) *param_bytes = 4 * n;
+    if (grad_bytes) *grad_bytes = 4 * n;
+    if (adam_bytes) *adam_bytes = 8 * n;
+    if (shadow_bytes) *shadow_bytes = 2 * n;
+    if (pad_bytes) *pad_bytes = pads * (4 + 4 + 8 + 2);
+    return FSDP_OK;
+}
+
+int fsdp_profile_enable(fsdp_unit* u, int on) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    u->profiling = on != 0;
+    return FSDP_OK;
+}
+
+int fsdp_profile_read(fsdp_unit* u, int kernel, double* total_ms, int64_t* launches) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    if (kernel < 0 || kernel >= FSDP_KERNEL_COUNT) return fail(FSDP_E_INVALID_ARG, "unknown kernel");
+    DeviceGuard dg(u->device);
+    double sum = 0.0;
+    int64_t n = 0;
+    for (const ProfRecord& r : u->prof) {
+        if (r.kind != kernel) continue;
+        cudaError_t e = cudaEventSynchronize(r.stop);
+        float ms = 0.f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
+        if (e != cudaSuccess) return cuda_fail(e, "profiler event");
+        sum += ms;
+        ++n;
+    }
+    if (total_ms) *total_ms = sum;
+    if (launches) *launches = n;
+    return FSDP_OK;
+}
+
+int fsdp_profile_reset(fsdp_unit* u) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    DeviceGuard dg(u->device);
+    for (auto& r : u->prof) {
+        cudaEventSynchronize(r.stop);
+        cudaEventDestroy(r.start);
+        cudaEventDestroy(r.stop);
+    }
+    u->prof.clear();
+    return FSDP_OK;
+}
+
+}  // extern "C"

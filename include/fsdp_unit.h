@@ -1,0 +1,248 @@
+/*
+ * fsdp_unit.h -- C ABI of the GB300 per-unit FSDP cycle.
+ *
+ * One FSDP unit (a group of parameters gathered and freed together) is sharded
+ * over N data-parallel ranks.  The ranks are virtual: their shard buffers all
+ * live in the memory of the one GPU that was current when the unit was
+ * created, and every "collective" is a memory-bound kernel on that GPU.
+ *
+ * Sources (page title, then section):
+ *  [FSDP]   "PyTorch FSDP: Experiences on Scaling Fully Sharded Data Parallel"
+ *  [HOOD]   "FSDP Under The Hood: ZeRO-3 The PyTorch Way"
+ *  [ARCH]   "FSDP Architecture"
+ *  [NOTE]   "FSDP (Fully Sharded Data Parallel)" concept note
+ *
+ * Conventions shared by every call
+ *  - Return value: FSDP_OK (0) or a negative FSDP_E_* code.  Arguments are
+ *    checked on the host before anything is enqueued; a call that fails its
+ *    checks changes nothing.  fsdp_last_error() gives a one-line reason for
+ *    the calling thread's most recent failure.  No call aborts or traps.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Calls that enqueue GPU work return without waiting.
+ *  - Device: a unit belongs to the device that was current at creation; every
+ *    call makes that device current for its duration and restores the
+ *    caller's device afterwards.
+ *  - Pointers named *_dev are device pointers (or managed memory) that the
+ *    caller owns and keeps alive until the enqueued work has finished.  The
+ *    library never keeps a caller pointer after a call returns.
+ *  - Hot-path buffers (gradients, the gathered output) must be 32-byte
+ *    aligned (FSDP_E_ALIGN otherwise); allocations from cudaMalloc or torch
+ *    always are.
+ *  - Element types: fp32 is IEEE binary32; bf16 is stored as uint16_t bit
+ *    patterns (the upper half of the binary32 pattern).
+ *  - A unit is not thread-safe; distinct units are independent.
+ */
+#ifndef FSDP_UNIT_H
+#define FSDP_UNIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FSDP_API __attribute__((visibility("default")))
+#else
+#define FSDP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define FSDP_OK             0
+#define FSDP_E_INVALID_ARG (-1)  /* bad shape, count, enum, null pointer   */
+#define FSDP_E_OOM         (-2)  /* device or host allocation failed        */
+#define FSDP_E_CUDA        (-3)  /* a CUDA runtime call or launch failed    */
+#define FSDP_E_STATE       (-4)  /* call not valid in the unit's state      */
+#define FSDP_E_ALIGN       (-5)  /* a buffer is not 32-byte aligned         */
+#define FSDP_E_CAPACITY    (-6)  /* caller's output array is too small      */
+
+/* ---- enums ------------------------------------------------------------ */
+/* FLAT: the FSDP1 FlatParameter.  All parameters are flattened (row-major)
+ *   and concatenated in the order given; rank k owns the contiguous elements
+ *   floor(kP/N) .. floor((k+1)P/N)-1, no padding ([ARCH], the GPU-k boundary
+ *   formula; [FSDP] section 3.2.1 and Figure 3 for flatten + concatenate).
+ * DIM0: FSDP2 per-parameter Shard(0).  Each parameter is chunked along dim 0
+ *   with torch.chunk semantics: ceil(m/N) rows per chunk, the last chunk
+ *   short, trailing ranks empty when there are fewer chunks than ranks
+ *   ([NOTE] "FSDP1 vs FSDP2"; [HOOD] section 2).  A rank's shard is its chunks
+ *   of every parameter, concatenated in parameter order. */
+#define FSDP_LAYOUT_FLAT 0
+#define FSDP_LAYOUT_DIM0 1
+
+#define FSDP_DTYPE_F32  0
+#define FSDP_DTYPE_BF16 1
+
+/* per-rank state a unit owns */
+#define FSDP_STATE_PARAM      0  /* fp32 sharded master parameters           */
+#define FSDP_STATE_GRAD       1  /* fp32 gradient shard (reduce-scatter out) */
+#define FSDP_STATE_EXP_AVG    2  /* fp32 AdamW first moment m                */
+#define FSDP_STATE_EXP_AVG_SQ 3  /* fp32 AdamW second moment v               */
+#define FSDP_STATE_SHADOW     4  /* bf16 copy of the master shard            */
+
+/* kernels the profiler times */
+#define FSDP_KERNEL_SHARD_IN       0
+#define FSDP_KERNEL_GATHER         1
+#define FSDP_KERNEL_REDUCE_SCATTER 2
+#define FSDP_KERNEL_ADAMW          3
+#define FSDP_KERNEL_COUNT          4
+
+/* ---- plain structs ------------------------------------------------------ */
+typedef struct fsdp_unit fsdp_unit;   /* opaque; one FlatParamHandle ([FSDP] section 4.2) */
+
+/* torch.optim.AdamW's hyper-parameters, as doubles (the update itself runs
+ * in fp32; see fsdp_adamw_step). */
+typedef struct {
+    double lr;
+    double beta1;
+    double beta2;
+    double eps;
+    double weight_decay;
+} fsdp_adamw_hp;
+
+typedef struct {
+    int layout;                /* FSDP_LAYOUT_FLAT or FSDP_LAYOUT_DIM0                */
+    int num_ranks;             /* N, 1 .. 1024                                        */
+    int grad_dtype;            /* dtype of the N full gradient buffers: F32 or BF16   */
+    int reshard_after_forward; /* nonzero: fsdp_step gathers twice ([FSDP] 5.4)       */
+} fsdp_unit_config;
+
+/* One contiguous piece of a rank's shard. */
+typedef struct {
+    int32_t rank;        /* owning virtual rank                                        */
+    int32_t param;       /* parameter index (DIM0); -1 for FLAT (may span parameters)  */
+    int64_t global_off;  /* first element in the unsharded flat buffer                 */
+    int64_t shard_off;   /* first element within the rank's packed shard (no padding)  */
+    int64_t arena_off;   /* first element within the rank's device arena (with pads)   */
+    int64_t len;         /* element count, >= 1                                        */
+} fsdp_segment;
+
+/* Parameter shapes are passed as `nparams`, `ndims[nparams]` (0..8; a 0-d
+ * parameter is one element) and `dims`, all parameters' dims concatenated
+ * (sum of ndims entries, each >= 0).  The unit's element count P must be >= 1. */
+
+/* ---- layout (host only; no GPU needed) --------------------------------- */
+
+/* The layout the unit would use: P (total elements), the number of segments,
+ * and the segments themselves (rank-major, in each rank's storage order).
+ * `segs` may be NULL to query the count only; otherwise `cap` bounds the
+ * number written (FSDP_E_CAPACITY if too small, with *nsegs set).
+ * Arena offsets place global index i and its arena slot at the same
+ * remainder modulo 32 elements. */
+FSDP_API int fsdp_plan_layout(int nparams, const int* ndims, const int64_t* dims,
+                     int layout, int num_ranks,
+                     int64_t* numel, int64_t* nsegs,
+                     fsdp_segment* segs, int64_t cap);
+
+/* ---- lifetime ----------------------------------------------------------- */
+
+/* Create a unit on the current device.  Allocates and zero-fills the N ranks'
+ * state (master, gradient shard, m, v: 4 bytes per owned element each; bf16
+ * shadow: 2 bytes; plus up to 31 alignment pad elements per segment) and a
+ * small device tile table.  Synchronous.  ([FSDP] section 3.2.1: the
+ * FlatParameter owns the storage of its shards.) */
+FSDP_API int fsdp_unit_create(int nparams, const int* ndims, const int64_t* dims,
+                     const fsdp_unit_config* cfg, fsdp_unit** out);
+
+/* Free everything the unit owns.  Synchronises the unit's device first.
+ * NULL is accepted. */
+FSDP_API int fsdp_unit_destroy(fsdp_unit* unit);
+
+/* ---- the per-unit cycle --------------------------------------------------- */
+
+/* Shard-in (FlatParameter construction, [FSDP] section 3.2.1): copy the full
+ * fp32 parameters into the N ranks' master shards per the layout, zero the
+ * gradient shards and m, v, set the bf16 shadow to the rounded master, and
+ * reset the step count to 0.  `params_dev[p]` is parameter p, contiguous
+ * row-major fp32 (may be NULL for a parameter with zero elements). */
+FSDP_API int fsdp_load_params(fsdp_unit* unit, const float* const* params_dev, void* stream);
+
+/* All-gather with the param_dtype cast ([FSDP] section 3.2.1 "communication
+ * layout": the gathered buffer is the shards concatenated in rank order, i.e.
+ * the unsharded FlatParameter; [FSDP] section 4.4: one fp32 -> bf16 cast per
+ * gather).  Writes out_bf16_dev[i] = RNE_bf16(master[i]) for all i in [0, P):
+ * one buffer, since every virtual rank's result is the same.  Rounding is
+ * IEEE round-to-nearest-even; NaN stays NaN. */
+FSDP_API int fsdp_allgather(fsdp_unit* unit, uint16_t* out_bf16_dev, void* stream);
+
+/* Reduce-scatter in fp32 ([ARCH] backward step 3: sum the ranks' gradients
+ * and give rank k only the slice of its shard; [HOOD] section 3: fp32
+ * reduction).  `grads_dev` is a HOST array of N device pointers; pointer r is
+ * rank r's full unsharded gradient, P elements of the unit's grad_dtype.
+ * For every i, with g_r upcast exactly to fp32:
+ *     acc = g_0[i]; acc = acc + g_r[i] for r = 1 .. N-1 (in that order);
+ *     grad_shard[i] = acc / N   (IEEE division)
+ * The gradient shards are overwritten. */
+FSDP_API int fsdp_reduce_scatter(fsdp_unit* unit, const void* const* grads_dev, void* stream);
+
+/* Local AdamW on every rank's shard ([ARCH]: each GPU updates its own shard
+ * from its own gradient and optimizer-state shards, no communication; [HOOD]
+ * appendix: torch.optim.AdamW).  Increments the step count t, then for every
+ * owned element, in fp32 with one rounding per operation:
+ *     p = p * fp32(1 - lr*wd)
+ *     m = fp32(beta1)*m + fp32(1-beta1)*g
+ *     v = fp32(beta2)*v + fp32(1-beta2)*(g*g)
+ *     p = p - fp32(lr/(1-beta1^t)) * (m / (sqrt(v / fp32(1-beta2^t)) + fp32(eps)))
+ *     shadow = RNE_bf16(p)
+ * The scalar constants are formed in double on the host and rounded once. */
+FSDP_API int fsdp_adamw_step(fsdp_unit* unit, const fsdp_adamw_hp* hp, void* stream);
+
+/* One unit step ([ARCH] the per-unit cycle; [FSDP] section 5.4): gather into
+ * out_bf16_dev (forward), gather again when reshard_after_forward is set
+ * (backward), reduce-scatter `grads_dev`, AdamW.  Same arguments and rules as
+ * the individual calls; all four are checked before any is enqueued. */
+FSDP_API int fsdp_step(fsdp_unit* unit, const void* const* grads_dev, uint16_t* out_bf16_dev,
+              const fsdp_adamw_hp* hp, void* stream);
+
+/* ---- state access (tests, checkpoint / resume) --------------------------- */
+
+/* Copy rank `rank`'s packed shard of state `which` (pads excluded; fp32, or
+ * bf16 for FSDP_STATE_SHADOW) to `dst`, or from `src` into the unit.  dst/src
+ * may be device or host memory (cudaMemcpyAsync with cudaMemcpyDefault; use
+ * pinned host memory for asynchrony).  Size = the rank's shard length. */
+FSDP_API int fsdp_get_state(const fsdp_unit* unit, int which, int rank, void* dst, void* stream);
+FSDP_API int fsdp_set_state(fsdp_unit* unit, int which, int rank, const void* src, void* stream);
+
+/* Copy elements [begin, begin+count) of state `which` in unsharded (global)
+ * order to `dst` (device or host). */
+FSDP_API int fsdp_read_global(const fsdp_unit* unit, int which, int64_t begin, int64_t count,
+                     void* dst, void* stream);
+
+/* AdamW step count t (0 after load). */
+FSDP_API int fsdp_get_step_count(const fsdp_unit* unit, int64_t* t);
+FSDP_API int fsdp_set_step_count(fsdp_unit* unit, int64_t t);
+
+/* ---- introspection --------------------------------------------------------- */
+
+FSDP_API int fsdp_unit_info(const fsdp_unit* unit, int64_t* numel, int* num_ranks, int* layout,
+                   int* grad_dtype, int* reshard_after_forward);
+
+/* The unit's segments (same contract as fsdp_plan_layout). */
+FSDP_API int fsdp_unit_segments(const fsdp_unit* unit, fsdp_segment* segs, int64_t cap, int64_t* nsegs);
+
+/* Steady-state bytes held for rank `rank` ([ARCH] memory breakdown: 4 bytes
+ * of parameters, 4 of gradient and 8 of Adam state per owned element), the
+ * bf16 shadow (2 per owned element) and the alignment pads of all five. */
+FSDP_API int fsdp_memory_report(const fsdp_unit* unit, int rank, int64_t* param_bytes,
+                       int64_t* grad_bytes, int64_t* adam_bytes, int64_t* shadow_bytes,
+                       int64_t* pad_bytes);
+
+/* ---- profiling ------------------------------------------------------------- */
+
+/* While enabled, every kernel the unit launches is bracketed by CUDA events
+ * recorded on its launch stream.  fsdp_profile_read waits for the recorded
+ * events and returns, for one FSDP_KERNEL_* kind, the summed device time in
+ * milliseconds and the launch count since the last reset.  Disabling keeps
+ * the records; fsdp_profile_reset drops them. */
+FSDP_API int fsdp_profile_enable(fsdp_unit* unit, int on);
+FSDP_API int fsdp_profile_read(fsdp_unit* unit, int kernel, double* total_ms, int64_t* launches);
+FSDP_API int fsdp_profile_reset(fsdp_unit* unit);
+
+/* ---- errors -------------------------------------------------------------- */
+FSDP_API const char* fsdp_strerror(int code);
+FSDP_API const char* fsdp_last_error(void);    /* calling thread's latest failure reason */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FSDP_UNIT_H */

@@ -1,0 +1,44 @@
+"""GPU parity at the full workload sizes, through fsdp_step (the call the bench
+times): whole units where the host holds them, sampled windows otherwise."""
+import pytest
+import torch
+
+from fully_sharded_unit_gb300 import workloads
+
+import gpu_harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from conftest import library
+    library()
+    yield
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("unit", [0, 11])
+def test_gpt2_small_flat_full(unit):
+    H.run_full(workloads.get("gpt2_small_flat"), unit=unit, use_step=True, gen_device="cuda")
+
+
+@pytest.mark.parametrize("unit", [0, 35])
+def test_gpt2_large_dim0_full(unit):
+    H.run_full(workloads.get("gpt2_large_dim0"), unit=unit, use_step=True, gen_device="cuda")
+
+
+@pytest.mark.parametrize("name", ["ragged_flat_n7", "ragged_dim0_n7"])
+def test_ragged_n7_full(name):
+    H.run_full(workloads.get(name), use_step=True, gen_device="cuda")
+
+
+@pytest.mark.parametrize("name", ["ragged_flat_n64", "ragged_dim0_n64"])
+def test_ragged_n64_windows(name):
+    H.run_windowed(workloads.get(name))
+
+
+@pytest.mark.parametrize("unit", [0, 1])
+def test_mingpt175b_windows(unit):
+    cmp = H.run_windowed(workloads.get("mingpt175b_flat"), unit=unit)
+    assert cmp.covered > 1_000_000
