@@ -167,6 +167,13 @@ def _workloads() -> dict:
         units=tuple(gpt_block(128, 512, n0006, n0006, n0006) for _ in range(2)),
         N=8, layout="flat", grad_dtype="bf16", steps=2, grad_std=1e-4,
         outlier_frac=1e-3, outlier_scale=1e3)
+    w["gpt_d3072_flat_bf16"] = Workload(
+        name="gpt_d3072_flat_bf16",
+        description="Reduced minGPT-shaped block d=3072 ffn 12288 (113,286,144 params), N=8, bf16 grads "
+                    "with outliers; a few GB on the device, every kernel's traffic far above L2",
+        units=(gpt_block(3072, 12288, n0006, n0006, n0006),),
+        N=8, layout="flat", grad_dtype="bf16", steps=2, grad_std=1e-4,
+        outlier_frac=1e-3, outlier_scale=1e3)
     w["gpt_mini_dim0"] = Workload(
         name="gpt_mini_dim0",
         description="Reduced GPT block d=128 ffn 512 x2 units, DIM0, N=8",
