@@ -165,3 +165,58 @@ def brute_unit_run(shapes, N, layout, params, grads_per_step, hp, raf=True):
                 p = f32(p - f32(step * f32(mm / den)))
                 master[k][j], m[k][j], v[k][j] = p, mm, vv
     return dict(gathers=gathers, gshards=gshards, master=master, m=m, v=v, ranges=ranges)
+
+
+def padded_ranges(P: int, N: int):
+    """Padded equal chunks: deal the P elements to ranks 0, 1, ... in blocks of
+    the smallest size c with c*N >= P; returns (begin, end, pads) per rank."""
+    c = 0
+    while c * N < P:
+        c += 1
+    out = []
+    pos = 0
+    for k in range(N):
+        take = min(c, P - pos)
+        out.append((pos, pos + take, c - take))
+        pos += take
+    return out
+
+
+def brute_reduce(grads, F=None, reduce_dtype="f32", old=None, inv_scale=1.0):
+    """Element-by-element reduction of W gradient lists of floats: group-wise
+    left folds (groups of F consecutive ranks; F = W is a single group), then
+    the fold over groups, then division by W; in bf16 arithmetic every result
+    is rounded to bf16; then the optional unscale and accumulation.  Returns
+    (values, found_nonfinite)."""
+    W = len(grads)
+    F = W if F is None else F
+    P = len(grads[0])
+    out = []
+    found = False
+
+    def rb(x):   # a double holding an fp32 value, rounded to bf16
+        if math.isnan(x) or math.isinf(x):
+            return x
+        return bits_f32(bf16_round(f32(x)) << 16)
+
+    for i in range(P):
+        if reduce_dtype == "bf16":
+            acc = rb(grads[0][i])
+            for r in range(1, W):
+                acc = rb(f32(acc + rb(grads[r][i])))
+            val = rb(f32(acc / W))
+        else:
+            tot = None
+            for g in range(W // F):
+                acc = f32(grads[g * F][i])
+                for r in range(1, F):
+                    acc = f32(acc + f32(grads[g * F + r][i]))
+                tot = acc if tot is None else f32(tot + acc)
+            val = f32(tot / W)
+        if inv_scale != 1.0:
+            val = f32(val * f32(inv_scale))
+        if old is not None:
+            val = f32(old[i] + val)
+        found = found or math.isnan(val) or math.isinf(val)
+        out.append(val)
+    return out, found

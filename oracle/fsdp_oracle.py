@@ -54,6 +54,7 @@ import numpy as np
 
 FLAT = "flat"
 DIM0 = "dim0"
+FLAT_PADDED = "flat_padded"
 
 F32 = np.float32
 
@@ -125,6 +126,9 @@ def rank_segments(shapes, N: int, layout: str, k: int):
     if layout == FLAT:
         a, b = flat_shard_range(P, N, k)
         return [(a, b)] if b > a else []
+    if layout == FLAT_PADDED:
+        a, b, _ = padded_shard_range(P, N, k)
+        return [(a, b)] if b > a else []
     if layout == DIM0:
         segs = []
         for s, off in zip(shapes, offs):
@@ -148,6 +152,13 @@ class Layout:
 
     def shard_len(self, k: int) -> int:
         return sum(b - a for a, b in self.segments[k])
+
+    def padding(self, k: int) -> int:
+        """Padding elements rank k stores after its real elements (padded
+        layout only; the other layouts store none)."""
+        if self.layout != FLAT_PADDED:
+            return 0
+        return padded_shard_range(self.P, self.N, k)[2]
 
 
 # --------------------------------------------------------------------------
@@ -253,6 +264,62 @@ def reduce_full(grads) -> np.ndarray:
     return (acc / F32(N)).astype(F32)
 
 
+def reduce_full_hybrid(grads, F: int) -> np.ndarray:
+    """Hybrid sharding ("PyTorch FSDP ...", section 3.2.2, Figure 4): the W
+    ranks form W/F sharding groups of F consecutive ranks; rank i*F + k is
+    rank k of group i.  The global sum is decomposed as
+        sum_r g_r = sum_i ( sum_{r in S_i} g_r ):
+    a reduce-scatter inside each sharding group (left fold over its F ranks in
+    order), then an all-reduce across groups (left fold over the group sums
+    in group order), then one division by W.  With F = W or F = 1 the fold
+    order is the plain rank order."""
+    W = len(grads)
+    assert W % F == 0
+    total = None
+    for i in range(W // F):
+        acc = upcast_grad(grads[i * F]).astype(F32, copy=True)
+        for r in range(1, F):
+            acc = (acc + upcast_grad(grads[i * F + r])).astype(F32)
+        total = acc if total is None else (total + acc).astype(F32)
+    return (total / F32(W)).astype(F32)
+
+
+def reduce_full_bf16(grads) -> np.ndarray:
+    """Reduction in bf16 (reduce_dtype = bf16, "PyTorch FSDP ...", section
+    4.4: collectives may run in the low precision).  Every rank's gradient is
+    first rounded to bf16 (exact when it already is bf16), every partial sum
+    is rounded to bf16, and so is the division by N; the result is widened
+    exactly to fp32 for the fp32 gradient shard.  Each bf16 operation is the
+    fp32 operation followed by one RNE rounding, which equals the correctly
+    rounded bf16 operation because fp32 carries more than 2*8+2 bits."""
+    N = len(grads)
+
+    def b(x):
+        return bf16_to_f32(bf16_rne(x))
+
+    acc = b(upcast_grad(grads[0]))
+    for r in range(1, N):
+        acc = b((acc + b(upcast_grad(grads[r]))).astype(F32))
+    return b((acc / F32(N)).astype(F32))
+
+
+def reduce_update(G, old=None, inv_scale: float = 1.0):
+    """Post-reduction steps on the reduced gradient G, in this order:
+    unscale (G * inv_scale, skipped when inv_scale is 1, as a loss-scaling
+    grad scaler does) and accumulation into the existing gradient shard
+    (old + G: gradient accumulation with communication, "PyTorch FSDP ...",
+    section 3.3.4: every micro-batch is reduce-scattered and each rank adds the
+    result to its local gradient shard).  Returns the new gradient values and
+    whether any of them is non-finite (the sharded grad scaler's global
+    overflow decision, section 4.4: the OR over all ranks' shards)."""
+    G = np.asarray(G, F32)
+    if inv_scale != 1.0:
+        G = (G * F32(inv_scale)).astype(F32)
+    if old is not None:
+        G = (np.asarray(old, F32) + G).astype(F32)
+    return G, bool((~np.isfinite(G)).any())
+
+
 def reduce_scatter(grads, lay: Layout):
     """Rank k's fp32 gradient shard: the reduced gradient restricted to rank
     k's segments (reduce, then keep only the matching slice)."""
@@ -345,9 +412,17 @@ class UnitOracle:
     ("FSDP Architecture", memory breakdown), plus 2 for the bf16 copy."""
 
     def __init__(self, shapes, N: int, layout: str, hp: AdamWHyper = AdamWHyper(),
-                 reshard_after_forward: bool = True):
+                 reshard_after_forward: bool = True, replicas: int = 1, reduce_dtype: str = "f32"):
+        """N is the sharding factor F (ranks a parameter is sharded over).
+        With replicas R > 1 the unit is hybrid-sharded over W = F*R ranks
+        ("PyTorch FSDP ...", section 3.2.2): the R members of a replication
+        group hold identical shards, so one copy of each shard is kept, and a
+        reduce-scatter takes W gradients ordered group by group."""
+        assert not (replicas > 1 and reduce_dtype != "f32"), "hybrid reduction is fp32"
         self.lay = Layout(list(shapes), N, layout)
         self.N = N
+        self.replicas = replicas
+        self.reduce_dtype = reduce_dtype
         self.hp = hp
         self.raf = reshard_after_forward
         self.t = 0
@@ -367,8 +442,20 @@ class UnitOracle:
     def allgather(self) -> np.ndarray:
         return allgather_cast(self.master, self.lay)
 
-    def reduce_scatter(self, grads):
-        self.grad = reduce_scatter(grads, self.lay)
+    def reduce_scatter(self, grads, accumulate: bool = False, inv_scale: float = 1.0) -> bool:
+        """Reduce the W = N*replicas gradients, keep each rank's slice (added to
+        its existing shard when accumulating).  Returns the found-non-finite flag."""
+        assert len(grads) == self.N * self.replicas
+        if self.replicas > 1:
+            G = reduce_full_hybrid(grads, self.N)
+        elif self.reduce_dtype == "bf16":
+            G = reduce_full_bf16(grads)
+        else:
+            G = reduce_full(grads)
+        old = unshard(self.grad, self.lay) if accumulate else None
+        G, found = reduce_update(G, old, inv_scale)
+        self.grad = shard(G, self.lay)
+        return found
 
     def adamw_step(self):
         self.t += 1

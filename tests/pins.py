@@ -249,3 +249,103 @@ def check_adamw_fp64(adamw_update, adamw_update_f64, hp, steps=5, seed=0):
     assert tol_ok(p, pd)
     assert np.all(np.abs(m - md) <= 1e-5 * M)
     assert tol_ok(v, vd, atol=0, rtol=1e-5)
+
+
+# ----------------------------------------------------------------- next rows
+
+def check_padded_vs_torch_chunk(padded_shard_range, cases):
+    """The padded equal-chunk layout's real elements are torch.chunk of the
+    flat buffer viewed as one 1-D tensor; every rank's chunk (real + pads) has
+    the same size and the total padding is at most N - 1."""
+    for P, N in cases:
+        chunks = torch.chunk(torch.arange(P), N)
+        c = chunks[0].numel()
+        pads = 0
+        for k in range(N):
+            a, b, pad = padded_shard_range(P, N, k)
+            if k < len(chunks):
+                assert (a, b) == (int(chunks[k][0]), int(chunks[k][-1]) + 1), (P, N, k)
+            else:
+                assert a == b
+            assert (b - a) + pad == c
+            pads += pad
+        assert pads <= N - 1 and pads == N * c - P
+
+
+def check_padded_vs_brute(padded_shard_range, Pmax=40, Nmax=20):
+    for P in range(1, Pmax + 1):
+        for N in range(1, Nmax + 1):
+            assert [tuple(padded_shard_range(P, N, k)) for k in range(N)] == brute.padded_ranges(P, N)
+
+
+def check_hybrid_reduce(reduce_full_hybrid, reduce_full, seed=0):
+    rng = np.random.default_rng(seed)
+    # integer-valued gradients: the decomposition is exact, mean (W+1)/2
+    for W, F in [(8, 2), (8, 4), (12, 3), (6, 6), (6, 1)]:
+        grads = [np.full(33, r + 1, np.float32) for r in range(W)]
+        assert np.all(reduce_full_hybrid(grads, F) == np.float32((W + 1) / 2))
+    # F = W (one sharding group) and F = 1 (pure replication) are the plain rank-order fold
+    for W in (1, 4, 7):
+        grads = [rng.normal(0, 1, 500).astype(np.float32) for _ in range(W)]
+        assert np.array_equal(reduce_full_hybrid(grads, W), reduce_full(grads))
+        assert np.array_equal(reduce_full_hybrid(grads, 1), reduce_full(grads))
+    # 1 < F < W groups the fold: ranks (1e8, 1 | -1e8, 0) with F = 2 give
+    # (1e8 + 1) + (-1e8 + 0) = 0 (the 1 is absorbed inside group 0), while
+    # ranks (1e8, -1e8 | 1, 0) give 0 + 1 = 1, mean 0.25
+    g = [np.array([x], np.float32) for x in (1e8, 1.0, -1e8, 0.0)]
+    assert reduce_full_hybrid(g, 2)[0] == np.float32(0.0)
+    g = [np.array([x], np.float32) for x in (1e8, -1e8, 1.0, 0.0)]
+    assert reduce_full_hybrid(g, 2)[0] == np.float32(0.25)
+    # the grouping is visible: ranks (1, 1e8 | -1e8, 1): F = 2 gives
+    # (1 + 1e8) + (-1e8 + 1) = 1e8 - 1e8 = 0; the plain fold gives ((1 + 1e8) - 1e8) + 1 = 1
+    g = [np.array([x], np.float32) for x in (1.0, 1e8, -1e8, 1.0)]
+    assert reduce_full_hybrid(g, 2)[0] == np.float32(0.0)
+    assert reduce_full(g)[0] == np.float32(0.25)
+    # within the fp64 bound of the exact mean
+    u = 2.0 ** -24
+    for W, F in [(8, 2), (16, 4)]:
+        grads = [rng.normal(0, 1e-3, 2048).astype(np.float32) for _ in range(W)]
+        G = reduce_full_hybrid(grads, F).astype(np.float64)
+        g64 = np.stack([x.astype(np.float64) for x in grads])
+        exact = g64.sum(0) / W
+        bound = (W - 1) * u * np.abs(g64).sum(0) / W * (1 + 1e-6) + u * np.abs(exact) * 1.0001
+        assert np.all(np.abs(G - exact) <= bound)
+
+
+def check_bf16_reduce_vs_torch(reduce_full_bf16, seed=0):
+    """torch CPU bfloat16 arithmetic (each op computed in fp32 and rounded to
+    bf16) folded in rank order, then divided by N."""
+    rng = np.random.default_rng(seed)
+    for N in (1, 2, 3, 7, 8):
+        grads = [rng.normal(0, 1e-2, 3000).astype(np.float32) for _ in range(N)]
+        acc = torch.from_numpy(grads[0]).to(torch.bfloat16)
+        for g in grads[1:]:
+            acc = acc + torch.from_numpy(g).to(torch.bfloat16)
+        want = (acc / N).to(torch.float32).numpy()
+        got = reduce_full_bf16(grads)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), N
+    # small integers are exact in bf16: mean (N+1)/2
+    for N in (2, 5, 8):
+        grads = [np.full(10, r + 1, np.float32) for r in range(N)]
+        assert np.all(reduce_full_bf16(grads) == np.float32((N + 1) / 2))
+
+
+def check_reduce_update(reduce_update):
+    # accumulation of k micro-batches: k * 2.5, exact
+    old = np.zeros(50, np.float32)
+    for k in range(1, 5):
+        old, found = reduce_update(np.full(50, 2.5, np.float32), old)
+        assert np.all(old == np.float32(2.5 * k)) and not found
+    # unscale by a power of two is exact; 1.0 is the identity
+    G = np.random.default_rng(0).normal(0, 1, 100).astype(np.float32)
+    assert np.array_equal(reduce_update(G, None, 0.25)[0], G / np.float32(4))
+    assert np.array_equal(reduce_update(G, None, 1.0)[0], G)
+    # the flag is the OR over every element: one inf or NaN anywhere sets it
+    for bad in (np.inf, -np.inf, np.nan):
+        H = G.copy()
+        H[37] = bad
+        assert reduce_update(H)[1]
+    assert not reduce_update(G)[1]
+    # overflow created by the unscale is found too
+    with np.errstate(over="ignore"):
+        assert reduce_update(np.array([3e38], np.float32), None, 4.0)[1]

@@ -112,3 +112,39 @@ def test_adamw_eps_inside_sqrt_caught():
         p2 = p1 - c["step"] * (m1 / np.sqrt(v1 / c["bc2"] + c["eps"]))
         return p2.astype(np.float32), m1.astype(np.float32), v1.astype(np.float32)
     _fails(pins.check_adamw_vs_torch, upd, HP)
+
+
+def test_padded_floor_instead_of_ceil_caught():
+    def r(P, N, k):
+        a, b = O.flat_shard_range(P, N, k)
+        return a, b, 0
+    _fails(pins.check_padded_vs_torch_chunk, r, [(15, 16), (5, 4)])
+
+
+def test_hybrid_flat_fold_caught():
+    _fails(pins.check_hybrid_reduce, lambda grads, F: O.reduce_full(grads), O.reduce_full)
+
+
+def test_hybrid_divide_by_group_size_caught():
+    def r(grads, F):
+        return (O.reduce_full_hybrid(grads, F) * np.float32(len(grads)) / np.float32(F)).astype(np.float32)
+    _fails(pins.check_hybrid_reduce, r, O.reduce_full)
+
+
+def test_bf16_reduce_in_fp32_caught():
+    def r(grads):
+        return O.bf16_to_f32(O.bf16_rne(O.reduce_full(grads)))
+    _fails(pins.check_bf16_reduce_vs_torch, r)
+
+
+def test_accumulate_overwrites_caught():
+    def upd(G, old=None, inv_scale=1.0):
+        return O.reduce_update(G, None, inv_scale)
+    _fails(pins.check_reduce_update, upd)
+
+
+def test_found_flag_misses_nan_caught():
+    def upd(G, old=None, inv_scale=1.0):
+        v, _ = O.reduce_update(G, old, inv_scale)
+        return v, bool(np.isinf(v).any())
+    _fails(pins.check_reduce_update, upd)
