@@ -28,8 +28,11 @@ FSDP_E_CAPACITY = -6
 
 FSDP_LAYOUT_FLAT = 0
 FSDP_LAYOUT_DIM0 = 1
+FSDP_LAYOUT_FLAT_PADDED = 2
 FSDP_DTYPE_F32 = 0
 FSDP_DTYPE_BF16 = 1
+FSDP_GATHER_FROM_MASTER = 0
+FSDP_GATHER_FROM_SHADOW = 1
 
 FSDP_STATE_PARAM = 0
 FSDP_STATE_GRAD = 1
@@ -43,8 +46,9 @@ FSDP_KERNEL_REDUCE_SCATTER = 2
 FSDP_KERNEL_ADAMW = 3
 FSDP_KERNEL_COUNT = 4
 
-LAYOUTS = {"flat": FSDP_LAYOUT_FLAT, "dim0": FSDP_LAYOUT_DIM0}
+LAYOUTS = {"flat": FSDP_LAYOUT_FLAT, "dim0": FSDP_LAYOUT_DIM0, "flat_padded": FSDP_LAYOUT_FLAT_PADDED}
 GRAD_DTYPES = {"f32": FSDP_DTYPE_F32, "bf16": FSDP_DTYPE_BF16}
+GATHER_SOURCES = {"master": FSDP_GATHER_FROM_MASTER, "shadow": FSDP_GATHER_FROM_SHADOW}
 STATES = {"param": FSDP_STATE_PARAM, "grad": FSDP_STATE_GRAD, "exp_avg": FSDP_STATE_EXP_AVG,
           "exp_avg_sq": FSDP_STATE_EXP_AVG_SQ, "shadow": FSDP_STATE_SHADOW}
 KERNELS = {"shard_in": FSDP_KERNEL_SHARD_IN, "gather": FSDP_KERNEL_GATHER,
@@ -63,7 +67,13 @@ class AdamWHp(ctypes.Structure):
 
 class UnitConfig(ctypes.Structure):
     _fields_ = [("layout", ctypes.c_int), ("num_ranks", ctypes.c_int), ("grad_dtype", ctypes.c_int),
-                ("reshard_after_forward", ctypes.c_int)]
+                ("reshard_after_forward", ctypes.c_int), ("replicas", ctypes.c_int),
+                ("reduce_dtype", ctypes.c_int), ("gather_source", ctypes.c_int)]
+
+
+class RSOptions(ctypes.Structure):
+    _fields_ = [("accumulate", ctypes.c_int), ("inv_scale", ctypes.c_double),
+                ("found_nonfinite_dev", ctypes.c_void_p)]
 
 
 class FsdpError(RuntimeError):
@@ -85,6 +95,8 @@ _SIGNATURES = {
     "fsdp_load_params": (_I, [_P, ctypes.POINTER(_P), _P]),
     "fsdp_allgather": (_I, [_P, _P, _P]),
     "fsdp_reduce_scatter": (_I, [_P, ctypes.POINTER(_P), _P]),
+    "fsdp_reduce_scatter_ex": (_I, [_P, ctypes.POINTER(_P), ctypes.POINTER(RSOptions), _P]),
+    "fsdp_zero_grad": (_I, [_P, _P]),
     "fsdp_adamw_step": (_I, [_P, ctypes.POINTER(AdamWHp), _P]),
     "fsdp_step": (_I, [_P, ctypes.POINTER(_P), _P, ctypes.POINTER(AdamWHp), _P]),
     "fsdp_get_state": (_I, [_P, _I, _I, _P, _P]),
@@ -92,7 +104,7 @@ _SIGNATURES = {
     "fsdp_read_global": (_I, [_P, _I, _I64, _I64, _P, _P]),
     "fsdp_get_step_count": (_I, [_P, _PI64]),
     "fsdp_set_step_count": (_I, [_P, _I64]),
-    "fsdp_unit_info": (_I, [_P, _PI64, _PI, _PI, _PI, _PI]),
+    "fsdp_unit_info": (_I, [_P, _PI64, ctypes.POINTER(UnitConfig)]),
     "fsdp_unit_segments": (_I, [_P, ctypes.POINTER(Segment), _I64, _PI64]),
     "fsdp_memory_report": (_I, [_P, _I, _PI64, _PI64, _PI64, _PI64, _PI64]),
     "fsdp_profile_enable": (_I, [_P, _I]),
@@ -169,10 +181,12 @@ def fsdp_plan_layout(shapes, layout, num_ranks):
     return P.value, list(segs)[:ns.value]
 
 
-def fsdp_unit_create(shapes, layout, num_ranks, grad_dtype="f32", reshard_after_forward=True):
+def fsdp_unit_create(shapes, layout, num_ranks, grad_dtype="f32", reshard_after_forward=True,
+                     replicas=1, reduce_dtype="f32", gather_source="master"):
     n, nd, dims = _shape_args(shapes)
     cfg = UnitConfig(LAYOUTS.get(layout, layout), int(num_ranks), GRAD_DTYPES.get(grad_dtype, grad_dtype),
-                     1 if reshard_after_forward else 0)
+                     1 if reshard_after_forward else 0, int(replicas),
+                     GRAD_DTYPES.get(reduce_dtype, reduce_dtype), GATHER_SOURCES.get(gather_source, gather_source))
     h = _P()
     _check(lib().fsdp_unit_create(n, nd, dims, ctypes.byref(cfg), ctypes.byref(h)), "fsdp_unit_create")
     return h
@@ -184,11 +198,11 @@ def fsdp_unit_destroy(h) -> None:
 
 def fsdp_unit_info(h):
     P = ctypes.c_int64()
-    N, lay, gd, raf = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    _check(lib().fsdp_unit_info(h, ctypes.byref(P), ctypes.byref(N), ctypes.byref(lay), ctypes.byref(gd),
-                                ctypes.byref(raf)), "fsdp_unit_info")
-    return dict(numel=P.value, num_ranks=N.value, layout=lay.value, grad_dtype=gd.value,
-                reshard_after_forward=bool(raf.value))
+    cfg = UnitConfig()
+    _check(lib().fsdp_unit_info(h, ctypes.byref(P), ctypes.byref(cfg)), "fsdp_unit_info")
+    return dict(numel=P.value, num_ranks=cfg.num_ranks, layout=cfg.layout, grad_dtype=cfg.grad_dtype,
+                reshard_after_forward=bool(cfg.reshard_after_forward), replicas=cfg.replicas,
+                reduce_dtype=cfg.reduce_dtype, gather_source=cfg.gather_source)
 
 
 def fsdp_unit_segments(h):
@@ -213,7 +227,7 @@ def fsdp_allgather(h, out: torch.Tensor, stream=None) -> None:
 
 def _check_grads(h, grads):
     info = fsdp_unit_info(h)
-    assert len(grads) == info["num_ranks"]
+    assert len(grads) == info["num_ranks"] * info["replicas"]
     want = torch.float32 if info["grad_dtype"] == FSDP_DTYPE_F32 else torch.bfloat16
     for g in grads:
         assert g.is_cuda and g.is_contiguous() and g.numel() >= info["numel"]
@@ -223,6 +237,21 @@ def _check_grads(h, grads):
 def fsdp_reduce_scatter(h, grads, stream=None) -> None:
     _check_grads(h, grads)
     _check(lib().fsdp_reduce_scatter(h, _ptrs(grads), _stream(stream)), "fsdp_reduce_scatter")
+
+
+def fsdp_reduce_scatter_ex(h, grads, accumulate=False, inv_scale=1.0, found: torch.Tensor | None = None,
+                           stream=None) -> None:
+    """``found``: optional one-element int32 CUDA tensor for the found-non-finite flag."""
+    _check_grads(h, grads)
+    if found is not None:
+        assert found.is_cuda and found.dtype == torch.int32 and found.numel() >= 1
+    opt = RSOptions(1 if accumulate else 0, float(inv_scale), found.data_ptr() if found is not None else None)
+    _check(lib().fsdp_reduce_scatter_ex(h, _ptrs(grads), ctypes.byref(opt), _stream(stream)),
+           "fsdp_reduce_scatter_ex")
+
+
+def fsdp_zero_grad(h, stream=None) -> None:
+    _check(lib().fsdp_zero_grad(h, _stream(stream)), "fsdp_zero_grad")
 
 
 def fsdp_adamw_step(h, hp, stream=None) -> None:
@@ -310,12 +339,15 @@ def fsdp_last_error() -> str:
 class Unit:
     """Owns one ``fsdp_unit`` handle; methods call the C entry points."""
 
-    def __init__(self, shapes, layout="flat", num_ranks=1, grad_dtype="f32", reshard_after_forward=True):
+    def __init__(self, shapes, layout="flat", num_ranks=1, grad_dtype="f32", reshard_after_forward=True,
+                 replicas=1, reduce_dtype="f32", gather_source="master"):
         self.shapes = [tuple(int(d) for d in s) for s in shapes]
-        self.handle = fsdp_unit_create(self.shapes, layout, num_ranks, grad_dtype, reshard_after_forward)
+        self.handle = fsdp_unit_create(self.shapes, layout, num_ranks, grad_dtype, reshard_after_forward,
+                                       replicas, reduce_dtype, gather_source)
         info = fsdp_unit_info(self.handle)
         self.numel = info["numel"]
         self.N = info["num_ranks"]
+        self.replicas = info["replicas"]
         self.grad_dtype = grad_dtype
         self.segments = fsdp_unit_segments(self.handle)
         self.shard_len = [0] * self.N
@@ -341,6 +373,12 @@ class Unit:
 
     def reduce_scatter(self, grads, stream=None):
         fsdp_reduce_scatter(self.handle, grads, stream)
+
+    def reduce_scatter_ex(self, grads, accumulate=False, inv_scale=1.0, found=None, stream=None):
+        fsdp_reduce_scatter_ex(self.handle, grads, accumulate, inv_scale, found, stream)
+
+    def zero_grad(self, stream=None):
+        fsdp_zero_grad(self.handle, stream)
 
     def adamw_step(self, hp, stream=None):
         fsdp_adamw_step(self.handle, hp, stream)

@@ -67,6 +67,9 @@ struct fsdp_unit {
     int nparams = 0;
     int grad_dtype = FSDP_DTYPE_F32;
     int raf = 1;
+    int replicas = 1;
+    int reduce_dtype = FSDP_DTYPE_F32;
+    int gather_source = FSDP_GATHER_FROM_MASTER;
     float* master = nullptr;
     float* grad = nullptr;
     float* m = nullptr;
@@ -77,7 +80,7 @@ struct fsdp_unit {
     Tile* load_tiles = nullptr;
     int64_t nload_tiles = 0;
     fsdp::ParamSrc* param_src = nullptr;
-    fsdp::KernelGrids grids{};
+    int sms = 1;
     int64_t t = 0;
     bool loaded = false;
     bool profiling = false;
@@ -162,7 +165,7 @@ int check_hp(const fsdp_adamw_hp* hp) {
 
 int check_grads(const fsdp_unit* u, const void* const* grads) {
     if (grads == nullptr) return fail(FSDP_E_INVALID_ARG, "grads array is null");
-    for (int r = 0; r < u->plan.N; ++r) {
+    for (int r = 0; r < u->plan.N * u->replicas; ++r) {
         if (grads[r] == nullptr) return fail(FSDP_E_INVALID_ARG, "a gradient pointer is null");
         if (!aligned32(grads[r])) return fail(FSDP_E_ALIGN, "a gradient buffer is not 32-byte aligned");
     }
@@ -192,14 +195,43 @@ fsdp::AdamWConsts adamw_consts(const fsdp_adamw_hp* hp, int64_t t) {
 
 int enqueue_gather(fsdp_unit* u, uint16_t* out, cudaStream_t st) {
     return profiled_launch(u, FSDP_KERNEL_GATHER, st, "gather launch", [&] {
-        return fsdp::launch_gather(u->tiles, u->ntiles, u->master, out, u->grids.gather, st);
+        if (u->gather_source == FSDP_GATHER_FROM_SHADOW)
+            return fsdp::launch_gather_shadow(u->tiles, u->ntiles, u->shadow, out, u->sms, st);
+        return fsdp::launch_gather(u->tiles, u->ntiles, u->master, out, u->sms, st);
     });
 }
 
-int enqueue_reduce_scatter(fsdp_unit* u, const void* const* grads, cudaStream_t st) {
+int check_rs_options(const fsdp_rs_options* opt) {
+    if (opt == nullptr) return FSDP_OK;
+    if (!std::isfinite(opt->inv_scale) || opt->inv_scale < 0)
+        return fail(FSDP_E_INVALID_ARG, "inv_scale must be finite and >= 0");
+    if (opt->found_nonfinite_dev != nullptr && (reinterpret_cast<uintptr_t>(opt->found_nonfinite_dev) & 3u))
+        return fail(FSDP_E_ALIGN, "found_nonfinite_dev is not 4-byte aligned");
+    return FSDP_OK;
+}
+
+int enqueue_reduce_scatter(fsdp_unit* u, const void* const* grads, const fsdp_rs_options* opt,
+                           cudaStream_t st) {
+    fsdp::ReduceArgs a{};
+    a.F = u->plan.N;
+    a.groups = u->replicas;
+    a.bf16_reduce = u->reduce_dtype == FSDP_DTYPE_BF16 ? 1 : 0;
+    a.inv_scale = 1.0f;
+    if (opt != nullptr) {
+        if (opt->inv_scale != 0.0 && opt->inv_scale != 1.0) {
+            a.scale = 1;
+            a.inv_scale = static_cast<float>(opt->inv_scale);
+        }
+        a.accumulate = opt->accumulate ? 1 : 0;
+        a.found = opt->found_nonfinite_dev;
+        if (a.found != nullptr) {
+            cudaError_t e = cudaMemsetAsync(a.found, 0, sizeof(int32_t), st);
+            if (e != cudaSuccess) return cuda_fail(e, "clearing the found-non-finite flag");
+        }
+    }
     return profiled_launch(u, FSDP_KERNEL_REDUCE_SCATTER, st, "reduce-scatter launch", [&] {
-        return fsdp::launch_reduce_scatter(u->tiles, u->ntiles, grads, u->plan.N, u->grad_dtype,
-                                           u->grad, u->grids.reduce_small, u->grids.reduce_large, st);
+        return fsdp::launch_reduce_scatter(u->tiles, u->ntiles, grads, u->grad_dtype, a, u->grad,
+                                           u->sms, st);
     });
 }
 
@@ -207,7 +239,7 @@ int enqueue_adamw(fsdp_unit* u, const fsdp_adamw_hp* hp, cudaStream_t st) {
     const fsdp::AdamWConsts c = adamw_consts(hp, u->t + 1);
     int rc = profiled_launch(u, FSDP_KERNEL_ADAMW, st, "AdamW launch", [&] {
         return fsdp::launch_adamw(u->plan.slab_len / 8, u->master, u->grad, u->m, u->v, u->shadow, c,
-                                  u->grids.adamw, st);
+                                  u->sms, st);
     });
     if (rc == FSDP_OK) u->t += 1;
     return rc;
@@ -254,6 +286,15 @@ int fsdp_unit_create(int nparams, const int* ndims, const int64_t* dims,
     *out = nullptr;
     if (cfg->grad_dtype != FSDP_DTYPE_F32 && cfg->grad_dtype != FSDP_DTYPE_BF16)
         return fail(FSDP_E_INVALID_ARG, "grad_dtype must be FSDP_DTYPE_F32 or FSDP_DTYPE_BF16");
+    if (cfg->reduce_dtype != FSDP_DTYPE_F32 && cfg->reduce_dtype != FSDP_DTYPE_BF16)
+        return fail(FSDP_E_INVALID_ARG, "reduce_dtype must be FSDP_DTYPE_F32 or FSDP_DTYPE_BF16");
+    if (cfg->gather_source != FSDP_GATHER_FROM_MASTER && cfg->gather_source != FSDP_GATHER_FROM_SHADOW)
+        return fail(FSDP_E_INVALID_ARG, "gather_source must be FSDP_GATHER_FROM_MASTER or _FROM_SHADOW");
+    const int replicas = cfg->replicas == 0 ? 1 : cfg->replicas;
+    if (replicas < 1 || cfg->num_ranks < 1 || replicas > fsdp::kMaxRanks / cfg->num_ranks)
+        return fail(FSDP_E_INVALID_ARG, "replicas must be >= 1 with num_ranks * replicas <= 1024");
+    if (replicas > 1 && cfg->reduce_dtype == FSDP_DTYPE_BF16)
+        return fail(FSDP_E_INVALID_ARG, "bf16 reduction is supported with replicas == 1 only");
     Plan plan;
     std::string err;
     int rc = fsdp::build_plan(nparams, ndims, dims, cfg->layout, cfg->num_ranks, &plan, &err);
@@ -269,6 +310,9 @@ int fsdp_unit_create(int nparams, const int* ndims, const int64_t* dims,
     u->nparams = nparams;
     u->grad_dtype = cfg->grad_dtype;
     u->raf = cfg->reshard_after_forward ? 1 : 0;
+    u->replicas = replicas;
+    u->reduce_dtype = cfg->reduce_dtype;
+    u->gather_source = cfg->gather_source;
 
     std::vector<Tile> tiles, load_tiles;
     fsdp::build_tiles(u->plan, &tiles);
@@ -307,7 +351,7 @@ int fsdp_unit_create(int nparams, const int* ndims, const int64_t* dims,
     if (e == cudaSuccess && !load_tiles.empty())
         e = cudaMemcpy(u->load_tiles, load_tiles.data(), load_tiles.size() * sizeof(Tile),
                        cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = fsdp::query_grids(u->device, u->grad_dtype, &u->grids);
+    if (e == cudaSuccess) e = fsdp::device_sms(u->device, &u->sms);
     if (e != cudaSuccess) {
         free_unit(u);
         delete u;
@@ -354,7 +398,7 @@ int fsdp_load_params(fsdp_unit* u, const float* const* params, void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "load set-up");
     rc = profiled_launch(u, FSDP_KERNEL_SHARD_IN, st, "shard-in launch", [&] {
         return fsdp::launch_shard_in(u->load_tiles, u->nload_tiles, u->param_src, u->master, u->shadow,
-                                     u->grids.shard_in, st);
+                                     u->sms, st);
     });
     if (rc) return rc;
     u->t = 0;
@@ -375,7 +419,26 @@ int fsdp_reduce_scatter(fsdp_unit* u, const void* const* grads, void* stream) {
     if (rc == FSDP_OK) rc = check_grads(u, grads);
     if (rc) return rc;
     DeviceGuard dg(u->device);
-    return enqueue_reduce_scatter(u, grads, static_cast<cudaStream_t>(stream));
+    return enqueue_reduce_scatter(u, grads, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int fsdp_reduce_scatter_ex(fsdp_unit* u, const void* const* grads, const fsdp_rs_options* opt,
+                           void* stream) {
+    int rc = check_unit(u, true);
+    if (rc == FSDP_OK) rc = check_grads(u, grads);
+    if (rc == FSDP_OK) rc = check_rs_options(opt);
+    if (rc) return rc;
+    DeviceGuard dg(u->device);
+    return enqueue_reduce_scatter(u, grads, opt, static_cast<cudaStream_t>(stream));
+}
+
+int fsdp_zero_grad(fsdp_unit* u, void* stream) {
+    int rc = check_unit(u, true);
+    if (rc) return rc;
+    DeviceGuard dg(u->device);
+    cudaError_t e = cudaMemsetAsync(u->grad, 0, static_cast<size_t>(u->plan.slab_len) * 4,
+                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "zeroing the gradient shards");
 }
 
 int fsdp_adamw_step(fsdp_unit* u, const fsdp_adamw_hp* hp, void* stream) {
@@ -397,7 +460,7 @@ int fsdp_step(fsdp_unit* u, const void* const* grads, uint16_t* out, const fsdp_
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     rc = enqueue_gather(u, out, st);                       // forward
     if (rc == FSDP_OK && u->raf) rc = enqueue_gather(u, out, st);   // backward re-gather
-    if (rc == FSDP_OK) rc = enqueue_reduce_scatter(u, grads, st);
+    if (rc == FSDP_OK) rc = enqueue_reduce_scatter(u, grads, nullptr, st);
     if (rc == FSDP_OK) rc = enqueue_adamw(u, hp, st);
     return rc;
 }
@@ -420,6 +483,11 @@ static int copy_state(const fsdp_unit* u, int which, int rank, void* ext, bool t
         cudaError_t e = to_unit ? cudaMemcpyAsync(dev, host, s.len * esz, cudaMemcpyDefault, st)
                                 : cudaMemcpyAsync(host, dev, s.len * esz, cudaMemcpyDefault, st);
         if (e != cudaSuccess) return cuda_fail(e, "state copy");
+    }
+    if (to_unit && which == FSDP_STATE_PARAM) {   // keep shadow == RNE(master)
+        cudaError_t e = fsdp::launch_cast_range(u->master, u->shadow, abase, u->plan.arena_len[rank],
+                                                u->sms, st);
+        if (e != cudaSuccess) return cuda_fail(e, "shadow refresh");
     }
     return FSDP_OK;
 }
@@ -474,15 +542,19 @@ int fsdp_set_step_count(fsdp_unit* u, int64_t t) {
     return FSDP_OK;
 }
 
-int fsdp_unit_info(const fsdp_unit* u, int64_t* numel, int* num_ranks, int* layout, int* grad_dtype,
-                   int* raf) {
+int fsdp_unit_info(const fsdp_unit* u, int64_t* numel, fsdp_unit_config* cfg) {
     int rc = check_unit(u, false);
     if (rc) return rc;
     if (numel) *numel = u->plan.P;
-    if (num_ranks) *num_ranks = u->plan.N;
-    if (layout) *layout = u->plan.layout;
-    if (grad_dtype) *grad_dtype = u->grad_dtype;
-    if (raf) *raf = u->raf;
+    if (cfg) {
+        cfg->layout = u->plan.layout;
+        cfg->num_ranks = u->plan.N;
+        cfg->grad_dtype = u->grad_dtype;
+        cfg->reshard_after_forward = u->raf;
+        cfg->replicas = u->replicas;
+        cfg->reduce_dtype = u->reduce_dtype;
+        cfg->gather_source = u->gather_source;
+    }
     return FSDP_OK;
 }
 

@@ -162,6 +162,48 @@ __global__ void __launch_bounds__(kBlock) gather_cast_kernel(const Tile* __restr
     }
 }
 
+// ---------------------------------------------------------------- gather from the shadow
+
+__global__ void __launch_bounds__(kBlock) gather_shadow_kernel(const Tile* __restrict__ tiles,
+                                                               int64_t ntiles,
+                                                               const uint16_t* __restrict__ shadow,
+                                                               uint16_t* __restrict__ out) {
+    const int tid = threadIdx.x;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const Tile tl = tiles[t];
+        const TileSplit sp = split_tile(tl.g, tl.len);
+        if (tid < sp.head) {
+            out[tl.g + tid] = shadow[tl.s + tid];
+        } else if (tid >= 8 && tid < 8 + sp.tail) {
+            const int j = sp.head + 8 * sp.nvec + (tid - 8);
+            out[tl.g + j] = shadow[tl.s + j];
+        }
+        const uint16_t* src = shadow + tl.s + sp.head;
+        uint16_t* dst = out + tl.g + sp.head;
+        uint4 r[kGroupsPerThread];
+#pragma unroll
+        for (int u = 0; u < kGroupsPerThread; ++u) {
+            const int v = tid + u * kBlock;
+            if (v < sp.nvec) r[u] = ld8bf_ro(src + 8 * v);
+        }
+#pragma unroll
+        for (int u = 0; u < kGroupsPerThread; ++u) {
+            const int v = tid + u * kBlock;
+            if (v < sp.nvec) st8bf(dst + 8 * v, r[u]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- range cast
+
+__global__ void __launch_bounds__(kBlock) cast_range_kernel(const float* __restrict__ master,
+                                                            uint16_t* __restrict__ shadow,
+                                                            int64_t n8) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; i < n8; i += stride)
+        st8bf(shadow + 8 * i, pack8(ld8_ro(master + 8 * i)));
+}
+
 // ---------------------------------------------------------------- reduce-scatter
 
 template <int NMAX>
@@ -208,13 +250,98 @@ struct GradIO<uint16_t> {
     }
 };
 
-template <typename GT, int NMAX>
+// fp32 value rounded to bf16 (RNE) and widened back: one bf16 rounding.
+__device__ __forceinline__ float round_bf16(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ bool not_finite(float x) {
+    return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;
+}
+
+// One element: group-wise left folds, the fold over groups, the division by W.
+template <typename GT, int NMAX, bool BF16>
+__device__ __forceinline__ float reduce1(const GradPtrs<NMAX>& gp, const ReduceArgs& a, int groups,
+                                         float fW, int64_t i) {
+    using IO = GradIO<GT>;
+    if (BF16) {
+        float acc = round_bf16(IO::load1(gp.p[0], i));
+        for (int r = 1; r < a.F; ++r) acc = round_bf16(__fadd_rn(acc, round_bf16(IO::load1(gp.p[r], i))));
+        return round_bf16(__fdiv_rn(acc, fW));
+    }
+    float tot = 0.f;
+    for (int grp = 0; grp < groups; ++grp) {
+        const int base = grp * a.F;
+        float acc = IO::load1(gp.p[base], i);
+        for (int r = 1; r < a.F; ++r) acc = __fadd_rn(acc, IO::load1(gp.p[base + r], i));
+        tot = grp == 0 ? acc : __fadd_rn(tot, acc);
+    }
+    return __fdiv_rn(tot, fW);
+}
+
+// Eight consecutive elements (an aligned group), same order of operations.
+template <typename GT, int NMAX, bool BF16>
+__device__ __forceinline__ F8 reduce8(const GradPtrs<NMAX>& gp, const ReduceArgs& a, int groups,
+                                      float fW, int64_t gi) {
+    using IO = GradIO<GT>;
+    F8 tot;
+    for (int grp = 0; grp < groups; ++grp) {
+        const int base = grp * a.F;
+        F8 acc;
+        for (int r0 = 0; r0 < a.F; r0 += kBatch) {
+            typename IO::Group x[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b)
+                if (r0 + b < a.F) x[b] = IO::load8(gp.p[base + r0 + b], gi);
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                if (r0 + b < a.F) {
+                    F8 w;
+                    IO::widen(x[b], w);
+                    if (BF16) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) w.v[e] = round_bf16(w.v[e]);
+                    }
+                    if (r0 + b == 0) {
+                        acc = w;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            acc.v[e] = __fadd_rn(acc.v[e], w.v[e]);
+                            if (BF16) acc.v[e] = round_bf16(acc.v[e]);
+                        }
+                    }
+                }
+            }
+        }
+        if (grp == 0) {
+            tot = acc;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) tot.v[e] = __fadd_rn(tot.v[e], acc.v[e]);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        tot.v[e] = __fdiv_rn(tot.v[e], fW);
+        if (BF16) tot.v[e] = round_bf16(tot.v[e]);
+    }
+    return tot;
+}
+
+// EXT = false compiles the plain reduce-scatter (one group, no unscale, no
+// accumulation, no flag) with the fewest registers; EXT = true adds hybrid
+// groups and the post-reduction options.
+template <typename GT, int NMAX, bool BF16, bool EXT>
 __global__ void __launch_bounds__(kBlock) reduce_scatter_kernel(const Tile* __restrict__ tiles,
                                                                 int64_t ntiles, GradPtrs<NMAX> gp,
-                                                                int N, float* __restrict__ gshard) {
-    using IO = GradIO<GT>;
+                                                                ReduceArgs a, float* __restrict__ gshard) {
     const int tid = threadIdx.x;
-    const float fN = static_cast<float>(N);
+    const int groups = EXT ? a.groups : 1;
+    const float fW = static_cast<float>(a.F * groups);
+    const bool post = EXT && (a.scale || a.accumulate);
+    int32_t* const found = EXT ? a.found : nullptr;
+    bool bad = false;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const Tile tl = tiles[t];
         const TileSplit sp = split_tile(tl.g, tl.len);
@@ -223,39 +350,35 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_kernel(const Tile* __re
         if (tid < sp.head) j = tid;
         else if (tid >= 8 && tid < 8 + sp.tail) j = sp.head + 8 * sp.nvec + (tid - 8);
         if (j >= 0) {
-            float acc = IO::load1(gp.p[0], tl.g + j);
-            for (int r = 1; r < N; ++r) acc = __fadd_rn(acc, IO::load1(gp.p[r], tl.g + j));
-            gshard[tl.s + j] = __fdiv_rn(acc, fN);
+            float x = reduce1<GT, NMAX, BF16>(gp, a, groups, fW, tl.g + j);
+            if (post && a.scale) x = __fmul_rn(x, a.inv_scale);
+            if (post && a.accumulate) x = __fadd_rn(gshard[tl.s + j], x);
+            if (found != nullptr) bad |= not_finite(x);
+            gshard[tl.s + j] = x;
         }
-        // 8-element groups: fold ranks 0..N-1 in order, kBatch loads in flight
+        // 8-element groups
         const int64_t g0 = tl.g + sp.head;
         float* dst = gshard + tl.s + sp.head;
         for (int v = tid; v < sp.nvec; v += kBlock) {
-            const int64_t gi = g0 + 8 * static_cast<int64_t>(v);
-            F8 acc;
-            for (int r0 = 0; r0 < N; r0 += kBatch) {
-                typename IO::Group x[kBatch];
+            F8 x = reduce8<GT, NMAX, BF16>(gp, a, groups, fW, g0 + 8 * static_cast<int64_t>(v));
+            if (post) {
+                F8 old;
+                if (a.accumulate) old = ld8_rw(dst + 8 * v);
 #pragma unroll
-                for (int b = 0; b < kBatch; ++b)
-                    if (r0 + b < N) x[b] = IO::load8(gp.p[r0 + b], gi);
-#pragma unroll
-                for (int b = 0; b < kBatch; ++b) {
-                    if (r0 + b < N) {
-                        F8 w;
-                        IO::widen(x[b], w);
-                        if (r0 + b == 0) {
-                            acc = w;
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc.v[e] = __fadd_rn(acc.v[e], w.v[e]);
-                        }
-                    }
+                for (int e = 0; e < 8; ++e) {
+                    if (a.scale) x.v[e] = __fmul_rn(x.v[e], a.inv_scale);
+                    if (a.accumulate) x.v[e] = __fadd_rn(old.v[e], x.v[e]);
                 }
             }
+            if (found != nullptr) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc.v[e] = __fdiv_rn(acc.v[e], fN);
-            st8(dst + 8 * v, acc);
+                for (int e = 0; e < 8; ++e) bad |= not_finite(x.v[e]);
+            }
+            st8(dst + 8 * v, x);
         }
+    }
+    if (found != nullptr) {   // uniform across the CTA
+        if (__syncthreads_or(bad) && tid == 0) *found = 1;
     }
 }
 
@@ -292,13 +415,13 @@ __global__ void __launch_bounds__(kBlock) adamw_kernel(int64_t n8, float* __rest
 }
 
 template <typename K>
-int resident_ctas(K kernel, int device, int sms) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBlock, 0) != cudaSuccess ||
-        per_sm < 1)
-        per_sm = 1;
-    (void)device;
-    return per_sm * sms;
+int per_sm(K kernel) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBlock, 0) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = 1;
+    }
+    return n;
 }
 
 int capped(int grid, int64_t work) {
@@ -308,63 +431,89 @@ int capped(int grid, int64_t work) {
 
 }  // namespace
 
-cudaError_t query_grids(int device, int grad_dtype, KernelGrids* out) {
-    int sms = 0;
-    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    if (e != cudaSuccess) return e;
-    out->gather = {resident_ctas(gather_cast_kernel, device, sms), kBlock};
-    if (grad_dtype == FSDP_DTYPE_BF16) {
-        out->reduce_small = {resident_ctas(reduce_scatter_kernel<uint16_t, 64>, device, sms), kBlock};
-        out->reduce_large = {resident_ctas(reduce_scatter_kernel<uint16_t, kMaxRanks>, device, sms), kBlock};
-    } else {
-        out->reduce_small = {resident_ctas(reduce_scatter_kernel<float, 64>, device, sms), kBlock};
-        out->reduce_large = {resident_ctas(reduce_scatter_kernel<float, kMaxRanks>, device, sms), kBlock};
-    }
-    out->adamw = {resident_ctas(adamw_kernel, device, sms), kBlock};
-    out->shard_in = {resident_ctas(shard_in_kernel, device, sms), kBlock};
-    return cudaGetLastError();
+cudaError_t device_sms(int device, int* sms) {
+    return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, device);
 }
 
 cudaError_t launch_shard_in(const Tile* tiles, int64_t ntiles, const ParamSrc* params,
-                            float* master, uint16_t* shadow, LaunchShape ls, cudaStream_t st) {
+                            float* master, uint16_t* shadow, int sms, cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
-    shard_in_kernel<<<capped(ls.grid, ntiles), kBlock, 0, st>>>(tiles, ntiles, params, master, shadow);
+    static const int occ = per_sm(shard_in_kernel);
+    shard_in_kernel<<<capped(occ * sms, ntiles), kBlock, 0, st>>>(tiles, ntiles, params, master, shadow);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather(const Tile* tiles, int64_t ntiles, const float* master, uint16_t* out,
-                          LaunchShape ls, cudaStream_t st) {
+                          int sms, cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
-    gather_cast_kernel<<<capped(ls.grid, ntiles), kBlock, 0, st>>>(tiles, ntiles, master, out);
+    static const int occ = per_sm(gather_cast_kernel);
+    gather_cast_kernel<<<capped(occ * sms, ntiles), kBlock, 0, st>>>(tiles, ntiles, master, out);
     return cudaGetLastError();
 }
 
-template <typename GT, int NMAX>
-static cudaError_t launch_rs_t(const Tile* tiles, int64_t ntiles, const void* const* grads, int N,
-                               float* gshard, LaunchShape ls, cudaStream_t st) {
-    GradPtrs<NMAX> gp;
-    for (int r = 0; r < NMAX; ++r) gp.p[r] = r < N ? grads[r] : nullptr;
-    reduce_scatter_kernel<GT, NMAX><<<capped(ls.grid, ntiles), kBlock, 0, st>>>(tiles, ntiles, gp, N, gshard);
+cudaError_t launch_gather_shadow(const Tile* tiles, int64_t ntiles, const uint16_t* shadow,
+                                 uint16_t* out, int sms, cudaStream_t st) {
+    if (ntiles == 0) return cudaSuccess;
+    static const int occ = per_sm(gather_shadow_kernel);
+    gather_shadow_kernel<<<capped(occ * sms, ntiles), kBlock, 0, st>>>(tiles, ntiles, shadow, out);
     return cudaGetLastError();
+}
+
+cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t begin, int64_t n,
+                              int sms, cudaStream_t st) {
+    const int64_t n8 = n / 8;
+    if (n8 == 0) return cudaSuccess;
+    static const int occ = per_sm(cast_range_kernel);
+    cast_range_kernel<<<capped(occ * sms, (n8 + kBlock - 1) / kBlock), kBlock, 0, st>>>(
+        master + begin, shadow + begin, n8);
+    return cudaGetLastError();
+}
+
+template <typename GT, int NMAX, bool BF16, bool EXT>
+static cudaError_t launch_rs_t(const Tile* tiles, int64_t ntiles, const void* const* grads,
+                               const ReduceArgs& a, float* gshard, int sms, cudaStream_t st) {
+    static const int occ = per_sm(reduce_scatter_kernel<GT, NMAX, BF16, EXT>);
+    GradPtrs<NMAX> gp;
+    const int W = a.F * a.groups;
+    for (int r = 0; r < NMAX; ++r) gp.p[r] = r < W ? grads[r] : nullptr;
+    reduce_scatter_kernel<GT, NMAX, BF16, EXT>
+        <<<capped(occ * sms, ntiles), kBlock, 0, st>>>(tiles, ntiles, gp, a, gshard);
+    return cudaGetLastError();
+}
+
+template <typename GT, int NMAX, bool BF16>
+static cudaError_t launch_rs_ext(const Tile* tiles, int64_t ntiles, const void* const* grads,
+                                 const ReduceArgs& a, float* gshard, int sms, cudaStream_t st) {
+    const bool ext = a.groups > 1 || a.scale || a.accumulate || a.found != nullptr;
+    return ext ? launch_rs_t<GT, NMAX, BF16, true>(tiles, ntiles, grads, a, gshard, sms, st)
+               : launch_rs_t<GT, NMAX, BF16, false>(tiles, ntiles, grads, a, gshard, sms, st);
+}
+
+template <typename GT>
+static cudaError_t launch_rs_dt(const Tile* tiles, int64_t ntiles, const void* const* grads,
+                                const ReduceArgs& a, float* gshard, int sms, cudaStream_t st) {
+    const bool small = a.F * a.groups <= 64;
+    if (a.bf16_reduce)
+        return small ? launch_rs_ext<GT, 64, true>(tiles, ntiles, grads, a, gshard, sms, st)
+                     : launch_rs_ext<GT, kMaxRanks, true>(tiles, ntiles, grads, a, gshard, sms, st);
+    return small ? launch_rs_ext<GT, 64, false>(tiles, ntiles, grads, a, gshard, sms, st)
+                 : launch_rs_ext<GT, kMaxRanks, false>(tiles, ntiles, grads, a, gshard, sms, st);
 }
 
 cudaError_t launch_reduce_scatter(const Tile* tiles, int64_t ntiles, const void* const* grads,
-                                  int N, int grad_dtype, float* gshard, LaunchShape small,
-                                  LaunchShape large, cudaStream_t st) {
+                                  int grad_dtype, const ReduceArgs& a, float* gshard, int sms,
+                                  cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
-    if (grad_dtype == FSDP_DTYPE_BF16) {
-        return N <= 64 ? launch_rs_t<uint16_t, 64>(tiles, ntiles, grads, N, gshard, small, st)
-                       : launch_rs_t<uint16_t, kMaxRanks>(tiles, ntiles, grads, N, gshard, large, st);
-    }
-    return N <= 64 ? launch_rs_t<float, 64>(tiles, ntiles, grads, N, gshard, small, st)
-                   : launch_rs_t<float, kMaxRanks>(tiles, ntiles, grads, N, gshard, large, st);
+    if (grad_dtype == FSDP_DTYPE_BF16) return launch_rs_dt<uint16_t>(tiles, ntiles, grads, a, gshard, sms, st);
+    return launch_rs_dt<float>(tiles, ntiles, grads, a, gshard, sms, st);
 }
 
 cudaError_t launch_adamw(int64_t n8, float* p, const float* g, float* m, float* v,
-                         uint16_t* shadow, const AdamWConsts& c, LaunchShape ls, cudaStream_t st) {
+                         uint16_t* shadow, const AdamWConsts& c, int sms, cudaStream_t st) {
     if (n8 == 0) return cudaSuccess;
+    static const int occ = per_sm(adamw_kernel);
     const int64_t blocks_needed = (n8 + kBlock - 1) / kBlock;
-    adamw_kernel<<<capped(ls.grid, blocks_needed), kBlock, 0, st>>>(n8, p, g, m, v, shadow, c);
+    adamw_kernel<<<capped(occ * sms, blocks_needed), kBlock, 0, st>>>(n8, p, g, m, v, shadow, c);
     return cudaGetLastError();
 }
 

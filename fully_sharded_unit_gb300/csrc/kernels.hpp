@@ -25,36 +25,43 @@ struct ParamSrc {
     int64_t offset;     // its FlatParameter offset
 };
 
-struct LaunchShape {
-    int grid;    // CTAs
-    int block;   // threads per CTA
+// Reduce-scatter arguments beyond the tile table and the gradient pointers.
+struct ReduceArgs {
+    int F;              // ranks per sharding group (the unit's N)
+    int groups;         // replication groups R >= 1; W = F*R gradients
+    int bf16_reduce;    // 1: bf16 arithmetic (requires groups == 1)
+    float inv_scale;    // multiplier applied when `scale` is set
+    int scale;
+    int accumulate;     // add into the existing gradient shard
+    int32_t* found;     // set to 1 when a written value is not finite; may be null
 };
 
-// Grid sizes: CTAs resident at once on the whole GPU (SMs x occupancy),
-// capped by the available work.
-struct KernelGrids {
-    LaunchShape gather;
-    LaunchShape reduce_small;   // N <= 64
-    LaunchShape reduce_large;   // N <= 1024
-    LaunchShape adamw;
-    LaunchShape shard_in;
-};
-
-cudaError_t query_grids(int device, int grad_dtype, KernelGrids* out);
+// Number of SMs of the unit's device; every kernel runs a persistent grid of
+// SMs x (CTAs resident per SM), capped by its work.
+cudaError_t device_sms(int device, int* sms);
 
 cudaError_t launch_shard_in(const Tile* tiles, int64_t ntiles, const ParamSrc* params,
-                            float* master, uint16_t* shadow, LaunchShape ls, cudaStream_t st);
+                            float* master, uint16_t* shadow, int sms, cudaStream_t st);
 
 cudaError_t launch_gather(const Tile* tiles, int64_t ntiles, const float* master,
-                          uint16_t* out, LaunchShape ls, cudaStream_t st);
+                          uint16_t* out, int sms, cudaStream_t st);
 
-// grads: N pointers (fp32 or bf16 per grad_dtype), each P elements.
+// The gather from the bf16 shadow shards (a copy; the cast was done by AdamW
+// or shard-in).
+cudaError_t launch_gather_shadow(const Tile* tiles, int64_t ntiles, const uint16_t* shadow,
+                                 uint16_t* out, int sms, cudaStream_t st);
+
+// grads: W = a.F * a.groups pointers (fp32 or bf16 per grad_dtype), each P elements.
 cudaError_t launch_reduce_scatter(const Tile* tiles, int64_t ntiles, const void* const* grads,
-                                  int N, int grad_dtype, float* gshard, LaunchShape small,
-                                  LaunchShape large, cudaStream_t st);
+                                  int grad_dtype, const ReduceArgs& a, float* gshard, int sms,
+                                  cudaStream_t st);
 
-// n8: number of 8-element groups in the slab (slab length / 8).
+// shadow[i] = RNE_bf16(master[i]) for i in [begin, begin + n); begin and n
+// multiples of 8.
+cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t begin, int64_t n,
+                              int sms, cudaStream_t st);
+
 cudaError_t launch_adamw(int64_t n8, float* p, const float* g, float* m, float* v,
-                         uint16_t* shadow, const AdamWConsts& c, LaunchShape ls, cudaStream_t st);
+                         uint16_t* shadow, const AdamWConsts& c, int sms, cudaStream_t st);
 
 }  // namespace fsdp

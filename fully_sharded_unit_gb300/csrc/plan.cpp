@@ -10,6 +10,10 @@
 //          Sharded Data Parallel)", FSDP1 vs FSDP2; "FSDP Under The Hood",
 //          section 2).  One segment per (rank, parameter) with a non-empty
 //          chunk, in parameter order within a rank.
+// FLAT_PADDED -- the FlatParameter right-padded to a multiple of N and cut
+//          into N chunks of ceil(P/N) ("PyTorch FSDP ...", section 3.2.1,
+//          Figure 3); rank k's real elements are [min(kc,P), min((k+1)c,P)) and
+//          its chunk ends with c - len zero padding elements, stored in its arena.
 //
 // Device arenas: each rank's arena starts at a multiple of kAlign in a slab
 // shared by all ranks, and every segment is placed so that its arena slot is
@@ -43,8 +47,8 @@ int build_plan(int nparams, const int* ndims, const int64_t* dims, int layout, i
         *err = "nparams must be >= 1 and ndims/out non-null";
         return FSDP_E_INVALID_ARG;
     }
-    if (layout != FSDP_LAYOUT_FLAT && layout != FSDP_LAYOUT_DIM0) {
-        *err = "layout must be FSDP_LAYOUT_FLAT or FSDP_LAYOUT_DIM0";
+    if (layout != FSDP_LAYOUT_FLAT && layout != FSDP_LAYOUT_DIM0 && layout != FSDP_LAYOUT_FLAT_PADDED) {
+        *err = "layout must be FSDP_LAYOUT_FLAT, FSDP_LAYOUT_DIM0 or FSDP_LAYOUT_FLAT_PADDED";
         return FSDP_E_INVALID_ARG;
     }
     if (N < 1 || N > kMaxRanks) {
@@ -104,6 +108,7 @@ int build_plan(int nparams, const int* ndims, const int64_t* dims, int layout, i
     }
 
     plan.shard_len.assign(N, 0);
+    plan.layout_pad.assign(N, 0);
     plan.arena_len.assign(N, 0);
     plan.arena_base.assign(N, 0);
     plan.rank_first_seg.assign(N + 1, 0);
@@ -126,6 +131,13 @@ int build_plan(int nparams, const int* ndims, const int64_t* dims, int layout, i
             int64_t a = floor_div_mul(k, plan.P, N);
             int64_t b = floor_div_mul(k + 1, plan.P, N);
             if (b > a) place(-1, a, b - a);
+        } else if (layout == FSDP_LAYOUT_FLAT_PADDED) {
+            const int64_t c = (plan.P + N - 1) / N;
+            const int64_t a = std::min<int64_t>(c * k, plan.P);
+            const int64_t b = std::min<int64_t>(c * (k + 1), plan.P);
+            if (b > a) place(-1, a, b - a);
+            plan.layout_pad[k] = c - (b - a);
+            cursor += plan.layout_pad[k];   // the chunk's zero padding
         } else {
             for (int p = 0; p < nparams; ++p) {
                 const ParamInfo& pi = plan.params[p];

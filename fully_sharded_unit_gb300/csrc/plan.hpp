@@ -37,6 +37,7 @@ struct Plan {
     std::vector<fsdp_segment> segs;     // rank-major, rank storage order
     std::vector<int64_t> rank_first_seg;  // N+1 entries: segs of rank k are [first[k], first[k+1])
     std::vector<int64_t> shard_len;     // per rank, owned elements
+    std::vector<int64_t> layout_pad;    // per rank, padding the layout stores (FLAT_PADDED)
     std::vector<int64_t> arena_len;     // per rank, multiple of kAlign
     std::vector<int64_t> arena_base;    // per rank, offset in the slab (multiple of kAlign)
     int64_t slab_len = 0;               // sum of arena_len

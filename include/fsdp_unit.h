@@ -69,9 +69,18 @@ extern "C" {
  *   of every parameter, concatenated in parameter order. */
 #define FSDP_LAYOUT_FLAT 0
 #define FSDP_LAYOUT_DIM0 1
+/* FLAT_PADDED: the FlatParameter as [FSDP] section 3.2.1 / Figure 3 builds it:
+ *   right-padded to a multiple of N and cut into N equal chunks of ceil(P/N)
+ *   elements; rank k owns [min(k*c, P), min((k+1)*c, P)) followed by zero
+ *   padding up to c elements (at most N-1 padding elements in all). */
+#define FSDP_LAYOUT_FLAT_PADDED 2
 
 #define FSDP_DTYPE_F32  0
 #define FSDP_DTYPE_BF16 1
+
+/* where the all-gather reads from */
+#define FSDP_GATHER_FROM_MASTER 0  /* fp32 master shard, cast to bf16 while gathering */
+#define FSDP_GATHER_FROM_SHADOW 1  /* bf16 shadow shard (always RNE(master)), copied  */
 
 /* per-rank state a unit owns */
 #define FSDP_STATE_PARAM      0  /* fp32 sharded master parameters           */
@@ -101,11 +110,32 @@ typedef struct {
 } fsdp_adamw_hp;
 
 typedef struct {
-    int layout;                /* FSDP_LAYOUT_FLAT or FSDP_LAYOUT_DIM0                */
-    int num_ranks;             /* N, 1 .. 1024                                        */
-    int grad_dtype;            /* dtype of the N full gradient buffers: F32 or BF16   */
-    int reshard_after_forward; /* nonzero: fsdp_step gathers twice ([FSDP] 5.4)       */
+    int layout;                /* FSDP_LAYOUT_FLAT, _DIM0 or _FLAT_PADDED                  */
+    int num_ranks;             /* N: ranks a parameter is sharded over (the sharding
+                                  factor F of [FSDP] 3.2.2), 1 .. 1024                     */
+    int grad_dtype;            /* dtype of the full gradient buffers: F32 or BF16         */
+    int reshard_after_forward; /* nonzero: fsdp_step gathers twice ([FSDP] 5.4)           */
+    int replicas;              /* hybrid sharding ([FSDP] 3.2.2): R >= 1 replication
+                                  groups; the data-parallel world is W = N*R ranks and a
+                                  reduce-scatter takes W gradients.  0 is read as 1.
+                                  N*R <= 1024.                                             */
+    int reduce_dtype;          /* F32 (default) or BF16 ([FSDP] 4.4: reductions in the
+                                  low precision); BF16 requires replicas == 1              */
+    int gather_source;         /* FSDP_GATHER_FROM_MASTER (default) or _FROM_SHADOW        */
 } fsdp_unit_config;
+
+/* Options of fsdp_reduce_scatter_ex; all-zero means a plain reduce-scatter. */
+typedef struct {
+    int accumulate;            /* nonzero: add the result to the existing gradient
+                                  shard (gradient accumulation with communication,
+                                  [FSDP] 3.3.4) instead of overwriting it               */
+    double inv_scale;          /* 0 or 1: no unscale; otherwise the reduced gradient is
+                                  multiplied by fp32(inv_scale) before accumulation
+                                  (loss-scale removal, [FSDP] 4.4 sharded grad scaler)  */
+    int32_t* found_nonfinite_dev; /* optional device int32: set to 1 if any written
+                                  gradient value is inf or NaN, else 0 (the global
+                                  overflow decision: an OR over every rank's shard)   */
+} fsdp_rs_options;
 
 /* One contiguous piece of a rank's shard. */
 typedef struct {
@@ -162,18 +192,37 @@ FSDP_API int fsdp_load_params(fsdp_unit* unit, const float* const* params_dev, v
  * the unsharded FlatParameter; [FSDP] section 4.4: one fp32 -> bf16 cast per
  * gather).  Writes out_bf16_dev[i] = RNE_bf16(master[i]) for all i in [0, P):
  * one buffer, since every virtual rank's result is the same.  Rounding is
- * IEEE round-to-nearest-even; NaN stays NaN. */
+ * IEEE round-to-nearest-even; NaN stays NaN.  With gather_source
+ * FSDP_GATHER_FROM_SHADOW the same bytes are copied from the bf16 shadow
+ * shards (which always hold RNE(master)): the gather then moves bf16, as when
+ * the collective runs in the low precision ([FSDP] 4.4). */
 FSDP_API int fsdp_allgather(fsdp_unit* unit, uint16_t* out_bf16_dev, void* stream);
 
-/* Reduce-scatter in fp32 ([ARCH] backward step 3: sum the ranks' gradients
- * and give rank k only the slice of its shard; [HOOD] section 3: fp32
- * reduction).  `grads_dev` is a HOST array of N device pointers; pointer r is
- * rank r's full unsharded gradient, P elements of the unit's grad_dtype.
- * For every i, with g_r upcast exactly to fp32:
- *     acc = g_0[i]; acc = acc + g_r[i] for r = 1 .. N-1 (in that order);
- *     grad_shard[i] = acc / N   (IEEE division)
+/* Reduce-scatter ([ARCH] backward step 3: sum the ranks' gradients and give
+ * rank k only the slice of its shard; [HOOD] section 3: fp32 reduction).
+ * `grads_dev` is a HOST array of W = N*replicas device pointers; pointer r is
+ * data-parallel rank r's full unsharded gradient, P elements of the unit's
+ * grad_dtype.  With replicas R, rank r = i*N + k is rank k of sharding group i.
+ * For every element, with g_r upcast exactly to fp32:
+ *   fp32 reduce:  acc_i = g_{iN} + g_{iN+1} + ... + g_{iN+N-1}   (left fold)
+ *                 tot   = acc_0 + acc_1 + ... + acc_{R-1}         (left fold)
+ *                 grad_shard = tot / W                            (IEEE division)
+ *     (R = 1 is the plain rank-order fold; the grouping is [FSDP] 3.2.2's
+ *     decomposition: reduce-scatter inside each sharding group, then all-reduce
+ *     across groups.)
+ *   bf16 reduce:  every input rounded to bf16, every partial sum and the
+ *     division by N rounded to bf16 (RNE), the result widened to fp32.
  * The gradient shards are overwritten. */
 FSDP_API int fsdp_reduce_scatter(fsdp_unit* unit, const void* const* grads_dev, void* stream);
+
+/* The same reduction followed, per element and in this order, by the
+ * optional unscale (x * fp32(inv_scale)) and accumulation (shard + x), and the
+ * optional found-non-finite flag over the values written.  `opt` may be NULL. */
+FSDP_API int fsdp_reduce_scatter_ex(fsdp_unit* unit, const void* const* grads_dev,
+                                    const fsdp_rs_options* opt, void* stream);
+
+/* Zero every rank's gradient shard (before the first accumulated micro-batch). */
+FSDP_API int fsdp_zero_grad(fsdp_unit* unit, void* stream);
 
 /* Local AdamW on every rank's shard ([ARCH]: each GPU updates its own shard
  * from its own gradient and optimizer-state shards, no communication; [HOOD]
@@ -199,7 +248,8 @@ FSDP_API int fsdp_step(fsdp_unit* unit, const void* const* grads_dev, uint16_t* 
 /* Copy rank `rank`'s packed shard of state `which` (pads excluded; fp32, or
  * bf16 for FSDP_STATE_SHADOW) to `dst`, or from `src` into the unit.  dst/src
  * may be device or host memory (cudaMemcpyAsync with cudaMemcpyDefault; use
- * pinned host memory for asynchrony).  Size = the rank's shard length. */
+ * pinned host memory for asynchrony).  Size = the rank's shard length.
+ * Setting FSDP_STATE_PARAM also recomputes that rank's shadow as RNE(master). */
 FSDP_API int fsdp_get_state(const fsdp_unit* unit, int which, int rank, void* dst, void* stream);
 FSDP_API int fsdp_set_state(fsdp_unit* unit, int which, int rank, const void* src, void* stream);
 
@@ -214,15 +264,18 @@ FSDP_API int fsdp_set_step_count(fsdp_unit* unit, int64_t t);
 
 /* ---- introspection --------------------------------------------------------- */
 
-FSDP_API int fsdp_unit_info(const fsdp_unit* unit, int64_t* numel, int* num_ranks, int* layout,
-                   int* grad_dtype, int* reshard_after_forward);
+/* The unit's element count P and the configuration it was created with
+ * (replicas normalised to >= 1). */
+FSDP_API int fsdp_unit_info(const fsdp_unit* unit, int64_t* numel, fsdp_unit_config* cfg);
 
 /* The unit's segments (same contract as fsdp_plan_layout). */
 FSDP_API int fsdp_unit_segments(const fsdp_unit* unit, fsdp_segment* segs, int64_t cap, int64_t* nsegs);
 
 /* Steady-state bytes held for rank `rank` ([ARCH] memory breakdown: 4 bytes
  * of parameters, 4 of gradient and 8 of Adam state per owned element), the
- * bf16 shadow (2 per owned element) and the alignment pads of all five. */
+ * bf16 shadow (2 per owned element) and the pads of all five (the padded
+ * layout's chunk padding plus alignment padding).  Under hybrid sharding this
+ * is one replica's copy; each of the R replicas holds the same. */
 FSDP_API int fsdp_memory_report(const fsdp_unit* unit, int rank, int64_t* param_bytes,
                        int64_t* grad_bytes, int64_t* adam_bytes, int64_t* shadow_bytes,
                        int64_t* pad_bytes);

@@ -39,7 +39,7 @@ def _check_against_oracle(shapes, N, layout):
             assert s.arena_off % 32 == s.global_off % 32    # alignment congruence
             assert s.arena_off >= prev_end and s.arena_off - prev_end < 32
             prev_end = s.arena_off + s.len
-            if layout == "flat":
+            if layout != "dim0":
                 assert s.param == -1
         assert pos == lay.shard_len(k)
     # segments listed rank-major
@@ -47,7 +47,7 @@ def _check_against_oracle(shapes, N, layout):
 
 
 @pytest.mark.parametrize("N", [1, 2, 3, 7, 8, 16, 64, 1024])
-@pytest.mark.parametrize("layout", ["flat", "dim0"])
+@pytest.mark.parametrize("layout", ["flat", "dim0", "flat_padded"])
 def test_plan_matches_oracle_random_shapes(N, layout):
     library()
     for shapes in SHAPE_SETS:
@@ -61,6 +61,13 @@ def test_plan_matches_oracle_workloads(name):
     library()
     wl = workloads.get(name)
     _check_against_oracle(wl.shapes(0), wl.N, wl.layout)
+
+
+@pytest.mark.parametrize("name", ["ragged_flat_n7", "ragged_flat_n64", "tiny_flat", "ragged_mini_flat_n3"])
+def test_padded_plan_matches_oracle_workloads(name):
+    library()
+    wl = workloads.get(name)
+    _check_against_oracle(wl.shapes(0), wl.N, "flat_padded")
 
 
 def test_plan_rejects_bad_arguments():
@@ -86,7 +93,11 @@ def test_create_rejects_bad_arguments_before_touching_the_gpu():
     library()
     for kw in [dict(shapes=[(4,)], layout="flat", num_ranks=0),
                dict(shapes=[(0,)], layout="dim0", num_ranks=2),
-               dict(shapes=[(4,)], layout="flat", num_ranks=2, grad_dtype=5)]:
+               dict(shapes=[(4,)], layout="flat", num_ranks=2, grad_dtype=5),
+               dict(shapes=[(4,)], layout="flat", num_ranks=2, replicas=-1),
+               dict(shapes=[(4,)], layout="flat", num_ranks=64, replicas=17),
+               dict(shapes=[(4,)], layout="flat", num_ranks=2, replicas=2, reduce_dtype="bf16"),
+               dict(shapes=[(4,)], layout="flat", num_ranks=2, gather_source=7)]:
         with pytest.raises(B.FsdpError) as e:
             B.fsdp_unit_create(**kw)
         assert e.value.code == B.FSDP_E_INVALID_ARG
