@@ -47,12 +47,15 @@ FALLBACK_HBM_GBS = 6800.0
 # --------------------------------------------------------------------------- helpers
 
 def counted_bytes(wl: workloads.Workload, unit: int) -> dict:
-    P, N = wl.unit_numel(unit), wl.N
+    """Algorithmic bytes of one unit step and of each kernel launch."""
+    P, W = wl.unit_numel(unit), wl.world
     gb = 4 if wl.grad_dtype == "f32" else 2
     R = 2 if wl.reshard_after_forward else 1
-    return dict(gather=6 * P, reduce_scatter=(N * gb + 4) * P, adamw=30 * P,
-                step=R * 6 * P + (N * gb + 4) * P + 30 * P, gathers=R,
-                h2d=N * gb * P, d2h=2 * P)
+    gather = (2 if wl.gather_source == "shadow" else 4) * P + 2 * P
+    rs = (W * gb + 4) * P
+    adamw = 30 * P
+    return dict(gather=gather, reduce_scatter=rs, adamw=adamw, step=R * gather + rs + adamw, gathers=R,
+                h2d=W * gb * P, d2h=2 * P)
 
 
 def measured_peak():
@@ -238,6 +241,13 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def selected_workload(args) -> workloads.Workload:
+    wl = workloads.get(args.workload)
+    over = {k: v for k, v in (("gather_source", args.gather_source), ("layout", args.layout),
+                              ("reduce_dtype", args.reduce_dtype)) if v is not None}
+    return wl.with_(**over) if over else wl
+
+
 def run_ours(args, world, rank, local):
     from fully_sharded_unit_gb300 import binding as B
     from fully_sharded_unit_gb300.build import build
@@ -248,11 +258,12 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     build()
     B.lib()
-    wl = workloads.get(args.workload)
+    wl = selected_workload(args)
     hp = workloads.hyper(wl)
     units = []
     for i in range(wl.n_units):
-        u = B.Unit(wl.shapes(i), wl.layout, wl.N, wl.grad_dtype, wl.reshard_after_forward)
+        u = B.Unit(wl.shapes(i), wl.layout, wl.N, wl.grad_dtype, wl.reshard_after_forward,
+                   replicas=wl.replicas, reduce_dtype=wl.reduce_dtype, gather_source=wl.gather_source)
         params = workloads.param_tensors(wl, i, dev)
         u.load(params)
         torch.cuda.synchronize()
@@ -260,8 +271,8 @@ def run_ours(args, world, rank, local):
         units.append(u)
     P_max = max(u.numel for u in units)
     # the N ranks' full gradients (one backward's output), reused by every unit
-    grads = [torch.empty(P_max, dtype=wl.torch_grad_dtype(), device=dev) for _ in range(wl.N)]
-    for r in range(wl.N):
+    grads = [torch.empty(P_max, dtype=wl.torch_grad_dtype(), device=dev) for _ in range(wl.world)]
+    for r in range(wl.world):
         workloads.grad_tensor(wl, 0, 0, r, dev, out=grads[r][:units[0].numel])
     out = torch.empty(P_max, dtype=torch.int16, device=dev)
     cb = [counted_bytes(wl, i) for i in range(wl.n_units)]
@@ -347,7 +358,9 @@ def run_ours(args, world, rank, local):
                    (wl.unit_numel(i) for i in range(wl.n_units))], "virtual_ranks": wl.N,
                    "layout": wl.layout, "grad_dtype": wl.grad_dtype,
                    "reshard_after_forward": wl.reshard_after_forward,
-                   "counted_bytes_per_step": step_bytes, "gather_source": "fp32 master",
+                   "replicas": wl.replicas, "reduce_dtype": wl.reduce_dtype,
+                   "counted_bytes_per_step": step_bytes,
+                   "gather_source": "fp32 master" if wl.gather_source == "master" else "bf16 shadow",
                    "l2": "inputs larger than L2; no flush", "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "clocks": clk.result,
@@ -404,6 +417,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    ap.add_argument("--gather-source", choices=["master", "shadow"], default=None,
+                    help="override the workload's gather source")
+    ap.add_argument("--layout", choices=["flat", "dim0", "flat_padded"], default=None)
+    ap.add_argument("--reduce-dtype", choices=["f32", "bf16"], default=None)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -53,6 +53,9 @@ class Workload:
     outlier_frac: float = 0.0
     outlier_scale: float = 1.0
     reshard_after_forward: bool = True
+    replicas: int = 1           # hybrid sharding: replication groups (W = N * replicas ranks)
+    reduce_dtype: str = "f32"   # "f32" | "bf16"
+    gather_source: str = "master"   # "master" (cast while gathering) | "shadow"
     seed: int = 0
     # AdamW hyper-parameters (torch.optim.AdamW argument names)
     lr: float = 1e-3
@@ -72,6 +75,11 @@ class Workload:
                 k *= d
             n += k
         return n
+
+    @property
+    def world(self) -> int:
+        """Data-parallel ranks that produce gradients (N * replicas)."""
+        return self.N * self.replicas
 
     @property
     def n_units(self) -> int:

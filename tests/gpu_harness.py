@@ -90,9 +90,11 @@ def run_full(wl: workloads.Workload, unit: int = 0, use_step: bool = False, step
     hp = workloads.hyper(wl)
     cmp = Comparison()
     params = workloads.param_tensors(wl, unit, gen_device)
-    orc = O.UnitOracle(shapes, N, wl.layout, O.AdamWHyper(**hp), wl.reshard_after_forward)
+    orc = O.UnitOracle(shapes, N, wl.layout, O.AdamWHyper(**hp), wl.reshard_after_forward,
+                       replicas=wl.replicas, reduce_dtype=wl.reduce_dtype)
     orc.load([p.cpu().numpy() for p in params])
-    u = B.Unit(shapes, wl.layout, N, wl.grad_dtype, wl.reshard_after_forward)
+    u = B.Unit(shapes, wl.layout, N, wl.grad_dtype, wl.reshard_after_forward, replicas=wl.replicas,
+               reduce_dtype=wl.reduce_dtype, gather_source=wl.gather_source)
     try:
         u.load([p.cuda() for p in params])
         del params
@@ -101,9 +103,9 @@ def run_full(wl: workloads.Workload, unit: int = 0, use_step: bool = False, step
             assert_bits_equal(u.get_state("param", k).cpu().numpy(), orc.master[k], f"shard-in rank {k}")
             assert_bits_equal(u16(u.get_state("shadow", k)), orc.shadow[k], f"shadow rank {k}")
         outs = [torch.empty(P, dtype=torch.int16, device="cuda") for _ in range(2)]
-        gdev = [torch.empty(P, dtype=wl.torch_grad_dtype(), device="cuda") for _ in range(N)]
+        gdev = [torch.empty(P, dtype=wl.torch_grad_dtype(), device="cuda") for _ in range(wl.world)]
         for s in range(steps):
-            for r in range(N):
+            for r in range(wl.world):
                 if gen_device == "cuda":
                     workloads.grad_tensor(wl, unit, s, r, "cuda", out=gdev[r])
                 else:
@@ -183,6 +185,7 @@ def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None
     times), compared on windows of global indices."""
     shapes = wl.shapes(unit)
     N, P = wl.N, wl.unit_numel(unit)
+    assert wl.replicas == 1 and wl.reduce_dtype == "f32", "windows use the plain fp32 reduction"
     steps = wl.steps if steps is None else steps
     hp = workloads.hyper(wl)
     lay = O.Layout(shapes, N, wl.layout)
@@ -191,7 +194,8 @@ def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None
     idx = _window_index(windows)
     idx_dev = idx.cuda()
     cmp = Comparison()
-    u = B.Unit(shapes, wl.layout, N, wl.grad_dtype, wl.reshard_after_forward)
+    u = B.Unit(shapes, wl.layout, N, wl.grad_dtype, wl.reshard_after_forward,
+               gather_source=wl.gather_source)
     try:
         params = workloads.param_tensors(wl, unit, "cuda")
         p_win = _flat_window(params, lay.offsets, idx.numpy())

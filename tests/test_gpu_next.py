@@ -1,0 +1,134 @@
+"""GPU parity for the rows beyond the basic cycle: padded equal-chunk FLAT
+layout, hybrid sharding, bf16 reduction, gather from the bf16 shadow,
+gradient accumulation with unscale and the found-non-finite flag."""
+import numpy as np
+import pytest
+import torch
+
+from fully_sharded_unit_gb300 import binding as B
+from fully_sharded_unit_gb300 import workloads
+from oracle import fsdp_oracle as O
+
+import gpu_harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from conftest import library
+    library()
+
+
+def _mini(layout="flat", N=7, **kw):
+    return workloads.get(f"ragged_mini_{'dim0' if layout == 'dim0' else 'flat'}_n{N}").with_(layout=layout, **kw)
+
+
+@pytest.mark.parametrize("N", [1, 3, 7, 64])
+def test_padded_layout(N):
+    H.run_full(_mini("flat_padded", N))
+    H.run_full(_mini("flat_padded", N), use_step=True, steps=2)
+
+
+def test_padded_layout_figure3_unit():
+    """Figure 3's Linear (12 weights + 3 bias) over 16 ranks: one element each."""
+    wl = workloads.Workload(
+        name="fig3", description="fig3",
+        units=((workloads.Param("w", (3, 4), ("normal", 0.1)), workloads.Param("b", (3,), ("normal", 0.1))),),
+        N=16, layout="flat_padded", grad_dtype="f32", steps=2, grad_std=1e-2)
+    H.run_full(wl)
+    u = B.Unit(wl.shapes(0), "flat_padded", 16)
+    try:
+        assert u.shard_len == [1] * 15 + [0]
+        assert [u.memory_report(k)["pad"] > 0 for k in range(16)][-1]
+    finally:
+        u.close()
+
+
+@pytest.mark.parametrize("layout,N,R", [("flat", 4, 2), ("dim0", 4, 2), ("flat", 8, 8), ("dim0", 3, 22),
+                                        ("flat", 1, 5)])
+def test_hybrid_sharding(layout, N, R):
+    H.run_full(_mini(layout, 7).with_(N=N, replicas=R))
+
+
+def test_hybrid_sharding_bf16_grads_through_step():
+    H.run_full(workloads.get("gpt_mini_flat_bf16").with_(N=4, replicas=2), use_step=True)
+
+
+@pytest.mark.parametrize("name", ["ragged_mini_flat_n8", "ragged_mini_dim0_n7", "gpt_mini_flat_bf16"])
+def test_bf16_reduction(name):
+    H.run_full(workloads.get(name).with_(reduce_dtype="bf16"))
+
+
+@pytest.mark.parametrize("name", ["ragged_mini_flat_n7", "ragged_mini_dim0_n64", "gpt_mini_flat_bf16"])
+def test_gather_from_shadow(name):
+    H.run_full(workloads.get(name).with_(gather_source="shadow"))
+    H.run_full(workloads.get(name).with_(gather_source="shadow"), use_step=True)
+
+
+def test_set_param_refreshes_the_shadow_gather():
+    wl = workloads.get("ragged_mini_flat_n7")
+    u = B.Unit(wl.shapes(0), "flat", 7, gather_source="shadow")
+    try:
+        u.load([p.cuda() for p in workloads.param_tensors(wl, 0)])
+        new = [torch.randn(u.shard_len[k], device="cuda") for k in range(7)]
+        for k in range(7):
+            u.set_state("param", k, new[k])
+        out = torch.empty(u.numel, dtype=torch.int16, device="cuda")
+        u.allgather(out)
+        torch.cuda.synchronize()
+        lay = O.Layout(wl.shapes(0), 7, "flat")
+        want = O.allgather_cast([x.cpu().numpy() for x in new], lay)
+        H.assert_bits_equal(H.u16(out), want, "gather after set_state")
+    finally:
+        u.close()
+
+
+@pytest.mark.parametrize("name,R", [("ragged_mini_flat_n7", 1), ("ragged_mini_dim0_n3", 1),
+                                    ("gpt_mini_flat_bf16", 1), ("ragged_mini_flat_n3", 2)])
+def test_accumulation_unscale_and_found_flag(name, R):
+    """Three micro-batches: the first overwrites, the next two accumulate with
+    an unscale; the flag reports non-finite values, including a planted NaN."""
+    wl = workloads.get(name).with_(replicas=R)
+    shapes, N, P = wl.shapes(0), wl.N, wl.unit_numel(0)
+    u = B.Unit(shapes, wl.layout, N, wl.grad_dtype, replicas=R)
+    orc = O.UnitOracle(shapes, N, wl.layout, replicas=R)
+    params = workloads.param_tensors(wl, 0)
+    orc.load([p.numpy() for p in params])
+    found = torch.empty(1, dtype=torch.int32, device="cuda")
+    try:
+        u.load([p.cuda() for p in params])
+        u.zero_grad()
+        for mb, (acc, scale) in enumerate([(False, 1.0), (True, 0.5), (True, 0.125)]):
+            grads = [workloads.grad_tensor(wl, 0, mb, r).cuda() for r in range(wl.world)]
+            if mb == 2:
+                grads[1][P // 2] = float("nan")
+            want_found = orc.reduce_scatter([H.grad_np(g) for g in grads], accumulate=acc, inv_scale=scale)
+            found.fill_(7)
+            u.reduce_scatter_ex(grads, accumulate=acc, inv_scale=scale, found=found)
+            torch.cuda.synchronize()
+            assert int(found.item()) == int(want_found), mb
+            for k in range(N):
+                H.assert_bits_equal(u.get_state("grad", k).cpu().numpy(), orc.grad[k], f"mb {mb} rank {k}")
+        assert want_found
+        u.zero_grad()
+        torch.cuda.synchronize()
+        assert not u.read_global("grad").any()
+    finally:
+        u.close()
+
+
+def test_overflow_from_unscale_sets_the_flag():
+    u = B.Unit([(1000,)], "flat", 2)
+    try:
+        u.load([torch.zeros(1000, device="cuda")])
+        g = [torch.full((1000,), 1e38, device="cuda"), torch.full((1000,), 1e38, device="cuda")]   # sum 2e38, mean 1e38
+        found = torch.zeros(1, dtype=torch.int32, device="cuda")
+        u.reduce_scatter_ex(g, inv_scale=0.5, found=found)
+        torch.cuda.synchronize()
+        assert int(found.item()) == 0
+        u.reduce_scatter_ex(g, inv_scale=4.0, found=found)
+        torch.cuda.synchronize()
+        assert int(found.item()) == 1
+    finally:
+        u.close()
