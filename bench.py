@@ -54,8 +54,11 @@ def counted_bytes(wl: workloads.Workload, unit: int) -> dict:
     gather = (2 if wl.gather_source == "shadow" else 4) * P + 2 * P
     rs = (W * gb + 4) * P
     adamw = 30 * P
-    return dict(gather=gather, reduce_scatter=rs, adamw=adamw, step=R * gather + rs + adamw, gathers=R,
-                h2d=W * gb * P, d2h=2 * P)
+    # fused: the gradient shard is written (4P) but not read back
+    reduce_adamw = (W * gb + 4 + 12 + 12 + 2) * P
+    step = R * gather + (reduce_adamw if wl.fuse_reduce_adamw else rs + adamw)
+    return dict(gather=gather, reduce_scatter=rs, adamw=adamw, reduce_adamw=reduce_adamw, step=step,
+                gathers=R, h2d=W * gb * P, d2h=2 * P)
 
 
 def measured_peak():
@@ -244,7 +247,9 @@ def run_reference(args, world, rank):
 def selected_workload(args) -> workloads.Workload:
     wl = workloads.get(args.workload)
     over = {k: v for k, v in (("gather_source", args.gather_source), ("layout", args.layout),
-                              ("reduce_dtype", args.reduce_dtype)) if v is not None}
+                              ("reduce_dtype", args.reduce_dtype),
+                              ("fuse_reduce_adamw", None if args.fuse is None else args.fuse == "on"))
+            if v is not None}
     return wl.with_(**over) if over else wl
 
 
@@ -263,7 +268,8 @@ def run_ours(args, world, rank, local):
     units = []
     for i in range(wl.n_units):
         u = B.Unit(wl.shapes(i), wl.layout, wl.N, wl.grad_dtype, wl.reshard_after_forward,
-                   replicas=wl.replicas, reduce_dtype=wl.reduce_dtype, gather_source=wl.gather_source)
+                   replicas=wl.replicas, reduce_dtype=wl.reduce_dtype, gather_source=wl.gather_source,
+                   fuse_reduce_adamw=wl.fuse_reduce_adamw)
         params = workloads.param_tensors(wl, i, dev)
         u.load(params)
         torch.cuda.synchronize()
@@ -309,7 +315,7 @@ def run_ours(args, world, rank, local):
     # per-kernel device time over the timed region (events on the launch stream)
     per_kernel = {}
     launches = 0
-    for k in ("gather", "reduce_scatter", "adamw"):
+    for k in ("gather", "reduce_scatter", "adamw", "reduce_adamw"):
         tot, n = 0.0, 0
         for u in units:
             t, c = B.fsdp_profile_read(u.handle, k)
@@ -359,6 +365,7 @@ def run_ours(args, world, rank, local):
                    "layout": wl.layout, "grad_dtype": wl.grad_dtype,
                    "reshard_after_forward": wl.reshard_after_forward,
                    "replicas": wl.replicas, "reduce_dtype": wl.reduce_dtype,
+                   "fused_reduce_adamw": wl.fuse_reduce_adamw,
                    "counted_bytes_per_step": step_bytes,
                    "gather_source": "fp32 master" if wl.gather_source == "master" else "bf16 shadow",
                    "l2": "inputs larger than L2; no flush", "parallelism": f"replicas x{world}"},
@@ -421,6 +428,8 @@ def main(argv=None):
                     help="override the workload's gather source")
     ap.add_argument("--layout", choices=["flat", "dim0", "flat_padded"], default=None)
     ap.add_argument("--reduce-dtype", choices=["f32", "bf16"], default=None)
+    ap.add_argument("--fuse", choices=["on", "off"], default=None,
+                    help="override whether fsdp_step fuses reduce-scatter and AdamW")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

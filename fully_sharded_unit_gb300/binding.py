@@ -44,7 +44,8 @@ FSDP_KERNEL_SHARD_IN = 0
 FSDP_KERNEL_GATHER = 1
 FSDP_KERNEL_REDUCE_SCATTER = 2
 FSDP_KERNEL_ADAMW = 3
-FSDP_KERNEL_COUNT = 4
+FSDP_KERNEL_REDUCE_ADAMW = 4
+FSDP_KERNEL_COUNT = 5
 
 LAYOUTS = {"flat": FSDP_LAYOUT_FLAT, "dim0": FSDP_LAYOUT_DIM0, "flat_padded": FSDP_LAYOUT_FLAT_PADDED}
 GRAD_DTYPES = {"f32": FSDP_DTYPE_F32, "bf16": FSDP_DTYPE_BF16}
@@ -52,7 +53,8 @@ GATHER_SOURCES = {"master": FSDP_GATHER_FROM_MASTER, "shadow": FSDP_GATHER_FROM_
 STATES = {"param": FSDP_STATE_PARAM, "grad": FSDP_STATE_GRAD, "exp_avg": FSDP_STATE_EXP_AVG,
           "exp_avg_sq": FSDP_STATE_EXP_AVG_SQ, "shadow": FSDP_STATE_SHADOW}
 KERNELS = {"shard_in": FSDP_KERNEL_SHARD_IN, "gather": FSDP_KERNEL_GATHER,
-           "reduce_scatter": FSDP_KERNEL_REDUCE_SCATTER, "adamw": FSDP_KERNEL_ADAMW}
+           "reduce_scatter": FSDP_KERNEL_REDUCE_SCATTER, "adamw": FSDP_KERNEL_ADAMW,
+           "reduce_adamw": FSDP_KERNEL_REDUCE_ADAMW}
 
 
 class Segment(ctypes.Structure):
@@ -68,7 +70,8 @@ class AdamWHp(ctypes.Structure):
 class UnitConfig(ctypes.Structure):
     _fields_ = [("layout", ctypes.c_int), ("num_ranks", ctypes.c_int), ("grad_dtype", ctypes.c_int),
                 ("reshard_after_forward", ctypes.c_int), ("replicas", ctypes.c_int),
-                ("reduce_dtype", ctypes.c_int), ("gather_source", ctypes.c_int)]
+                ("reduce_dtype", ctypes.c_int), ("gather_source", ctypes.c_int),
+                ("fuse_reduce_adamw", ctypes.c_int)]
 
 
 class RSOptions(ctypes.Structure):
@@ -182,11 +185,12 @@ def fsdp_plan_layout(shapes, layout, num_ranks):
 
 
 def fsdp_unit_create(shapes, layout, num_ranks, grad_dtype="f32", reshard_after_forward=True,
-                     replicas=1, reduce_dtype="f32", gather_source="master"):
+                     replicas=1, reduce_dtype="f32", gather_source="master", fuse_reduce_adamw=False):
     n, nd, dims = _shape_args(shapes)
     cfg = UnitConfig(LAYOUTS.get(layout, layout), int(num_ranks), GRAD_DTYPES.get(grad_dtype, grad_dtype),
                      1 if reshard_after_forward else 0, int(replicas),
-                     GRAD_DTYPES.get(reduce_dtype, reduce_dtype), GATHER_SOURCES.get(gather_source, gather_source))
+                     GRAD_DTYPES.get(reduce_dtype, reduce_dtype), GATHER_SOURCES.get(gather_source, gather_source),
+                     1 if fuse_reduce_adamw else 0)
     h = _P()
     _check(lib().fsdp_unit_create(n, nd, dims, ctypes.byref(cfg), ctypes.byref(h)), "fsdp_unit_create")
     return h
@@ -202,7 +206,8 @@ def fsdp_unit_info(h):
     _check(lib().fsdp_unit_info(h, ctypes.byref(P), ctypes.byref(cfg)), "fsdp_unit_info")
     return dict(numel=P.value, num_ranks=cfg.num_ranks, layout=cfg.layout, grad_dtype=cfg.grad_dtype,
                 reshard_after_forward=bool(cfg.reshard_after_forward), replicas=cfg.replicas,
-                reduce_dtype=cfg.reduce_dtype, gather_source=cfg.gather_source)
+                reduce_dtype=cfg.reduce_dtype, gather_source=cfg.gather_source,
+                fuse_reduce_adamw=bool(cfg.fuse_reduce_adamw))
 
 
 def fsdp_unit_segments(h):
@@ -340,10 +345,10 @@ class Unit:
     """Owns one ``fsdp_unit`` handle; methods call the C entry points."""
 
     def __init__(self, shapes, layout="flat", num_ranks=1, grad_dtype="f32", reshard_after_forward=True,
-                 replicas=1, reduce_dtype="f32", gather_source="master"):
+                 replicas=1, reduce_dtype="f32", gather_source="master", fuse_reduce_adamw=False):
         self.shapes = [tuple(int(d) for d in s) for s in shapes]
         self.handle = fsdp_unit_create(self.shapes, layout, num_ranks, grad_dtype, reshard_after_forward,
-                                       replicas, reduce_dtype, gather_source)
+                                       replicas, reduce_dtype, gather_source, fuse_reduce_adamw)
         info = fsdp_unit_info(self.handle)
         self.numel = info["numel"]
         self.N = info["num_ranks"]

@@ -70,6 +70,7 @@ struct fsdp_unit {
     int replicas = 1;
     int reduce_dtype = FSDP_DTYPE_F32;
     int gather_source = FSDP_GATHER_FROM_MASTER;
+    int fuse = 0;
     float* master = nullptr;
     float* grad = nullptr;
     float* m = nullptr;
@@ -235,6 +236,22 @@ int enqueue_reduce_scatter(fsdp_unit* u, const void* const* grads, const fsdp_rs
     });
 }
 
+int enqueue_reduce_adamw(fsdp_unit* u, const void* const* grads, const fsdp_adamw_hp* hp,
+                         cudaStream_t st) {
+    fsdp::ReduceArgs a{};
+    a.F = u->plan.N;
+    a.groups = u->replicas;
+    a.bf16_reduce = u->reduce_dtype == FSDP_DTYPE_BF16 ? 1 : 0;
+    a.inv_scale = 1.0f;
+    const fsdp::AdamWConsts c = adamw_consts(hp, u->t + 1);
+    int rc = profiled_launch(u, FSDP_KERNEL_REDUCE_ADAMW, st, "fused reduce-scatter + AdamW launch", [&] {
+        return fsdp::launch_reduce_adamw(u->tiles, u->ntiles, grads, u->grad_dtype, a, u->grad, u->master,
+                                         u->m, u->v, u->shadow, c, st);
+    });
+    if (rc == FSDP_OK) u->t += 1;
+    return rc;
+}
+
 int enqueue_adamw(fsdp_unit* u, const fsdp_adamw_hp* hp, cudaStream_t st) {
     const fsdp::AdamWConsts c = adamw_consts(hp, u->t + 1);
     int rc = profiled_launch(u, FSDP_KERNEL_ADAMW, st, "AdamW launch", [&] {
@@ -313,6 +330,7 @@ int fsdp_unit_create(int nparams, const int* ndims, const int64_t* dims,
     u->replicas = replicas;
     u->reduce_dtype = cfg->reduce_dtype;
     u->gather_source = cfg->gather_source;
+    u->fuse = cfg->fuse_reduce_adamw ? 1 : 0;
 
     std::vector<Tile> tiles, load_tiles;
     fsdp::build_tiles(u->plan, &tiles);
@@ -460,6 +478,7 @@ int fsdp_step(fsdp_unit* u, const void* const* grads, uint16_t* out, const fsdp_
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     rc = enqueue_gather(u, out, st);                       // forward
     if (rc == FSDP_OK && u->raf) rc = enqueue_gather(u, out, st);   // backward re-gather
+    if (rc == FSDP_OK && u->fuse) return enqueue_reduce_adamw(u, grads, hp, st);
     if (rc == FSDP_OK) rc = enqueue_reduce_scatter(u, grads, nullptr, st);
     if (rc == FSDP_OK) rc = enqueue_adamw(u, hp, st);
     return rc;
@@ -554,6 +573,7 @@ int fsdp_unit_info(const fsdp_unit* u, int64_t* numel, fsdp_unit_config* cfg) {
         cfg->replicas = u->replicas;
         cfg->reduce_dtype = u->reduce_dtype;
         cfg->gather_source = u->gather_source;
+        cfg->fuse_reduce_adamw = u->fuse;
     }
     return FSDP_OK;
 }

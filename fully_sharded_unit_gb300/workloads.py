@@ -56,6 +56,7 @@ class Workload:
     replicas: int = 1           # hybrid sharding: replication groups (W = N * replicas ranks)
     reduce_dtype: str = "f32"   # "f32" | "bf16"
     gather_source: str = "master"   # "master" (cast while gathering) | "shadow"
+    fuse_reduce_adamw: bool = False  # fsdp_step runs reduce-scatter and AdamW as one kernel
     seed: int = 0
     # AdamW hyper-parameters (torch.optim.AdamW argument names)
     lr: float = 1e-3

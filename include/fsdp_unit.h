@@ -94,7 +94,8 @@ extern "C" {
 #define FSDP_KERNEL_GATHER         1
 #define FSDP_KERNEL_REDUCE_SCATTER 2
 #define FSDP_KERNEL_ADAMW          3
-#define FSDP_KERNEL_COUNT          4
+#define FSDP_KERNEL_REDUCE_ADAMW   4   /* fused reduce-scatter + AdamW (fsdp_step) */
+#define FSDP_KERNEL_COUNT          5
 
 /* ---- plain structs ------------------------------------------------------ */
 typedef struct fsdp_unit fsdp_unit;   /* opaque; one FlatParamHandle ([FSDP] section 4.2) */
@@ -122,6 +123,9 @@ typedef struct {
     int reduce_dtype;          /* F32 (default) or BF16 ([FSDP] 4.4: reductions in the
                                   low precision); BF16 requires replicas == 1              */
     int gather_source;         /* FSDP_GATHER_FROM_MASTER (default) or _FROM_SHADOW        */
+    int fuse_reduce_adamw;     /* nonzero: fsdp_step runs its reduce-scatter and AdamW as
+                                  one pass per element (the gradient shard is written and
+                                  used without being read back); results are identical   */
 } fsdp_unit_config;
 
 /* Options of fsdp_reduce_scatter_ex; all-zero means a plain reduce-scatter. */
@@ -239,7 +243,8 @@ FSDP_API int fsdp_adamw_step(fsdp_unit* unit, const fsdp_adamw_hp* hp, void* str
 /* One unit step ([ARCH] the per-unit cycle; [FSDP] section 5.4): gather into
  * out_bf16_dev (forward), gather again when reshard_after_forward is set
  * (backward), reduce-scatter `grads_dev`, AdamW.  Same arguments and rules as
- * the individual calls; all four are checked before any is enqueued. */
+ * the individual calls; all four are checked before any is enqueued.  With
+ * fuse_reduce_adamw the last two run as one kernel with the same results. */
 FSDP_API int fsdp_step(fsdp_unit* unit, const void* const* grads_dev, uint16_t* out_bf16_dev,
               const fsdp_adamw_hp* hp, void* stream);
 

@@ -94,7 +94,8 @@ def run_full(wl: workloads.Workload, unit: int = 0, use_step: bool = False, step
                        replicas=wl.replicas, reduce_dtype=wl.reduce_dtype)
     orc.load([p.cpu().numpy() for p in params])
     u = B.Unit(shapes, wl.layout, N, wl.grad_dtype, wl.reshard_after_forward, replicas=wl.replicas,
-               reduce_dtype=wl.reduce_dtype, gather_source=wl.gather_source)
+               reduce_dtype=wl.reduce_dtype, gather_source=wl.gather_source,
+               fuse_reduce_adamw=wl.fuse_reduce_adamw)
     try:
         u.load([p.cuda() for p in params])
         del params
@@ -195,7 +196,7 @@ def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None
     idx_dev = idx.cuda()
     cmp = Comparison()
     u = B.Unit(shapes, wl.layout, N, wl.grad_dtype, wl.reshard_after_forward,
-               gather_source=wl.gather_source)
+               gather_source=wl.gather_source, fuse_reduce_adamw=wl.fuse_reduce_adamw)
     try:
         params = workloads.param_tensors(wl, unit, "cuda")
         p_win = _flat_window(params, lay.offsets, idx.numpy())

@@ -42,3 +42,11 @@ def test_ragged_n64_windows(name):
 def test_mingpt175b_windows(unit):
     cmp = H.run_windowed(workloads.get("mingpt175b_flat"), unit=unit)
     assert cmp.covered > 1_000_000
+
+
+def test_mingpt175b_windows_fused_shadow_gather():
+    """The fastest configuration of the bench workload: fsdp_step with the fused
+    reduce-scatter + AdamW kernel and the gather from the bf16 shadow."""
+    wl = workloads.get("mingpt175b_flat").with_(fuse_reduce_adamw=True, gather_source="shadow")
+    cmp = H.run_windowed(wl, unit=0)
+    assert cmp.covered > 1_000_000

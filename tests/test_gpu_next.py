@@ -132,3 +132,32 @@ def test_overflow_from_unscale_sets_the_flag():
         assert int(found.item()) == 1
     finally:
         u.close()
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("ragged_mini_flat_n7", {}), ("ragged_mini_dim0_n64", {}), ("gpt_mini_flat_bf16", {}),
+    ("ragged_mini_flat_n3", {"replicas": 2}), ("ragged_mini_dim0_n8", {"reduce_dtype": "bf16"}),
+    ("ragged_mini_flat_n7", {"gather_source": "shadow", "layout": "flat_padded"}),
+    ("ragged_mini_flat_n64", {"reshard_after_forward": False}),
+])
+def test_fused_reduce_adamw_step(name, kw):
+    """fsdp_step with the reduce-scatter and AdamW fused into one kernel gives
+    the oracle's results bit for bit (the same operation sequence)."""
+    cmp = H.run_full(workloads.get(name).with_(fuse_reduce_adamw=True, **kw), use_step=True)
+    assert cmp.total_diff == 0
+
+
+def test_fused_step_profiles_one_kernel():
+    wl = workloads.get("ragged_mini_flat_n8")
+    u = B.Unit(wl.shapes(0), "flat", 8, fuse_reduce_adamw=True)
+    try:
+        u.load([p.cuda() for p in workloads.param_tensors(wl, 0)])
+        grads = [workloads.grad_tensor(wl, 0, 0, r).cuda() for r in range(8)]
+        out = torch.empty(wl.unit_numel(0), dtype=torch.int16, device="cuda")
+        B.fsdp_profile_enable(u.handle, True)
+        u.step(grads, out, workloads.hyper(wl))
+        counts = {k: B.fsdp_profile_read(u.handle, k)[1] for k in B.KERNELS}
+        assert counts == {"shard_in": 0, "gather": 2, "reduce_scatter": 0, "adamw": 0, "reduce_adamw": 1}
+        assert u.step_count == 1
+    finally:
+        u.close()
