@@ -376,21 +376,50 @@ def run_ours(args, world, rank, local):
 
 
 def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world):
-    """Same metric through the public API with the gradients in pinned host
-    memory: every step copies each unit's N gradients host->device, runs
-    fsdp_step, and copies the gathered bf16 parameters device->host."""
+    """Same metric through the public API with the step's inputs and result in
+    pinned host memory.  Every step, for every unit, the N gradients come from
+    the host and the gathered bf16 parameters go back to the host:
+      zero_copy -- fsdp_step reads the pinned host gradients directly over the
+                   host link (device addresses from fsdp_host_device_pointer);
+      copy      -- cudaMemcpyAsync of each gradient host->device first.
+    The device->host copy of a unit's gathered parameters runs on a second
+    stream, overlapping the next unit's step; the timed region ends when the
+    last copy has landed."""
+    from fully_sharded_unit_gb300 import binding as B
     P_max = grads[0].numel()
     host_grads = [torch.empty(P_max, dtype=grads[0].dtype, pin_memory=True) for _ in grads]
     for h, g in zip(host_grads, grads):
         h.copy_(g)
-    host_out = torch.empty(P_max, dtype=torch.int16, pin_memory=True)
+    host_out = [torch.empty(P_max, dtype=torch.int16, pin_memory=True) for _ in units]
+    outs = [out, torch.empty_like(out)]
+    copy_stream = torch.cuda.Stream(device=dev)
+    if args.e2e_mode == "zero_copy":
+        unit_grads = [[B.fsdp_host_device_pointer(h[:u.numel]) for h in host_grads] for u in units]
+    else:
+        unit_grads = [[g[:u.numel] for g in grads] for u in units]
+    free = [None, None]      # events: last D2H copy out of outs[k] finished
 
     def step():
-        for u in units:
-            for h, g in zip(host_grads, grads):
-                g[:u.numel].copy_(h[:u.numel], non_blocking=True)
-            u.step([g[:u.numel] for g in grads], out, hp, stream)
-            host_out[:u.numel].copy_(out[:u.numel], non_blocking=True)
+        done = []
+        for i, u in enumerate(units):
+            o = outs[i % 2]
+            if free[i % 2] is not None:
+                stream.wait_event(free[i % 2])
+            if args.e2e_mode == "copy":
+                for h, g in zip(host_grads, grads):
+                    g[:u.numel].copy_(h[:u.numel], non_blocking=True)
+            u.step(unit_grads[i], o, hp, stream)
+            ready = torch.cuda.Event()
+            ready.record(stream)
+            copy_stream.wait_event(ready)
+            with torch.cuda.stream(copy_stream):
+                host_out[i][:u.numel].copy_(o[:u.numel], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(copy_stream)
+            free[i % 2] = ev
+            done.append(ev)
+        for ev in done:
+            stream.wait_event(ev)
 
     step()
     torch.cuda.synchronize()
@@ -406,10 +435,10 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world)
     ms = dist_max(ev0.elapsed_time(ev1), world, dev)
     h2d = sum(c["h2d"] for c in cb)
     d2h = sum(c["d2h"] for c in cb)
-    del host_grads, host_out
+    del host_grads, host_out, unit_grads
     return {"value": world * step_bytes * args.e2e_steps / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "ms_per_step": ms / args.e2e_steps}
+            "ms_per_step": ms / args.e2e_steps, "mode": args.e2e_mode}
 
 
 def main(argv=None):
@@ -420,6 +449,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mingpt175b_flat", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-mode", choices=["zero_copy", "copy"], default="zero_copy")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -113,6 +113,7 @@ _SIGNATURES = {
     "fsdp_profile_enable": (_I, [_P, _I]),
     "fsdp_profile_read": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), _PI64]),
     "fsdp_profile_reset": (_I, [_P]),
+    "fsdp_host_device_pointer": (_I, [_P, ctypes.POINTER(_P)]),
     "fsdp_strerror": (ctypes.c_char_p, [_I]),
     "fsdp_last_error": (ctypes.c_char_p, []),
 }
@@ -329,6 +330,32 @@ def fsdp_profile_read(h, kernel):
 
 def fsdp_profile_reset(h) -> None:
     _check(lib().fsdp_profile_reset(h), "fsdp_profile_reset")
+
+
+class DevicePtr:
+    """A raw device address standing in for a tensor in calls that take buffers."""
+
+    def __init__(self, addr: int, like: torch.Tensor):
+        self.addr = addr
+        self.dtype = like.dtype
+        self.is_cuda = True
+        self._like = like          # keeps the host memory alive
+
+    def data_ptr(self) -> int:
+        return self.addr
+
+    def numel(self) -> int:
+        return self._like.numel()
+
+    def is_contiguous(self) -> bool:
+        return self._like.is_contiguous()
+
+
+def fsdp_host_device_pointer(host: torch.Tensor) -> DevicePtr:
+    """Device view of a pinned host tensor (read over the host link)."""
+    d = _P()
+    _check(lib().fsdp_host_device_pointer(host.data_ptr(), ctypes.byref(d)), "fsdp_host_device_pointer")
+    return DevicePtr(d.value, host)
 
 
 def fsdp_strerror(code: int) -> str:

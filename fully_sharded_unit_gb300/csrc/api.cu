@@ -281,6 +281,25 @@ const char* fsdp_strerror(int code) {
 
 const char* fsdp_last_error(void) { return g_last_error.c_str(); }
 
+int fsdp_host_device_pointer(const void* host, void** dev) {
+    if (host == nullptr || dev == nullptr) return fail(FSDP_E_INVALID_ARG, "host/dev is null");
+    *dev = nullptr;
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, host);
+    if (e != cudaSuccess || attr.type != cudaMemoryTypeHost) {
+        cudaGetLastError();
+        return fail(FSDP_E_INVALID_ARG, "not pinned host memory known to CUDA");
+    }
+    void* d = nullptr;
+    e = cudaHostGetDevicePointer(&d, const_cast<void*>(host), 0);
+    if (e != cudaSuccess || d == nullptr) {
+        cudaGetLastError();
+        return fail(FSDP_E_INVALID_ARG, std::string("no device mapping: ") + cudaGetErrorString(e));
+    }
+    *dev = d;
+    return FSDP_OK;
+}
+
 int fsdp_plan_layout(int nparams, const int* ndims, const int64_t* dims, int layout, int num_ranks,
                      int64_t* numel, int64_t* nsegs, fsdp_segment* segs, int64_t cap) {
     Plan plan;

@@ -296,6 +296,15 @@ FSDP_API int fsdp_profile_enable(fsdp_unit* unit, int on);
 FSDP_API int fsdp_profile_read(fsdp_unit* unit, int kernel, double* total_ms, int64_t* launches);
 FSDP_API int fsdp_profile_reset(fsdp_unit* unit);
 
+/* ---- host-resident buffers -------------------------------------------------- */
+
+/* Device address of pinned (page-locked, mapped) host memory, e.g. from
+ * cudaHostAlloc or a pinned torch tensor.  Gradient buffers given to
+ * fsdp_reduce_scatter / fsdp_step may live there: the reduce-scatter then reads
+ * them straight over the host link, with no staging copy.  Returns
+ * FSDP_E_INVALID_ARG if `host` is not pinned, mapped host memory. */
+FSDP_API int fsdp_host_device_pointer(const void* host, void** dev);
+
 /* ---- errors -------------------------------------------------------------- */
 FSDP_API const char* fsdp_strerror(int code);
 FSDP_API const char* fsdp_last_error(void);    /* calling thread's latest failure reason */

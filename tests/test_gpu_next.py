@@ -161,3 +161,32 @@ def test_fused_step_profiles_one_kernel():
         assert u.step_count == 1
     finally:
         u.close()
+
+
+def test_gradients_in_pinned_host_memory():
+    """Gradients read straight from pinned host memory give the same reduce-
+    scatter and step as device-resident ones."""
+    wl = workloads.get("gpt_mini_flat_bf16")
+    shapes, N, P = wl.shapes(0), wl.N, wl.unit_numel(0)
+    params = [p.cuda() for p in workloads.param_tensors(wl, 0)]
+    grads = [workloads.grad_tensor(wl, 0, 0, r) for r in range(N)]
+    host = [g.pin_memory() for g in grads]
+    views = [B.fsdp_host_device_pointer(h) for h in host]
+    a = B.Unit(shapes, "flat", N, "bf16", fuse_reduce_adamw=True)
+    b = B.Unit(shapes, "flat", N, "bf16", fuse_reduce_adamw=True)
+    try:
+        a.load(params)
+        b.load(params)
+        out_a = torch.empty(P, dtype=torch.int16, device="cuda")
+        out_b = torch.empty(P, dtype=torch.int16, device="cuda")
+        a.step([g.cuda() for g in grads], out_a, workloads.hyper(wl))
+        b.step(views, out_b, workloads.hyper(wl))
+        torch.cuda.synchronize()
+        for w in ("param", "grad", "exp_avg", "exp_avg_sq", "shadow"):
+            assert torch.equal(a.read_global(w), b.read_global(w)), w
+    finally:
+        a.close()
+        b.close()
+    with pytest.raises(B.FsdpError) as e:
+        B.fsdp_host_device_pointer(torch.zeros(16))          # pageable, not pinned
+    assert e.value.code == B.FSDP_E_INVALID_ARG
