@@ -418,47 +418,70 @@ __global__ void __launch_bounds__(kBlock) adamw_kernel(int64_t n8, float* __rest
 
 // One pass per element of the unit: the reduce-scatter result (any group
 // count, fp32 or bf16 reduction; no unscale, accumulation or flag) is written
-// to the gradient shard and immediately used by the AdamW update, so the
-// shard is not read back.  Same operation sequence as the two separate
-// kernels, so the results are identical; only segment elements are touched
-// (pads stay zero, which AdamW would preserve anyway).
-template <typename GT, int NMAX, bool BF16>
-__global__ void __launch_bounds__(kBlock) reduce_adamw_kernel(const Tile* __restrict__ tiles,
+// to the gradient shard and used by the AdamW update without being read back
+// from HBM.  Two phases per tile: phase 1 reduces the thread's 8-element
+// groups into shared memory (and writes the gradient shard), phase 2 runs
+// AdamW on the same groups reading G back from shared memory.  A thread reads
+// only the slots it wrote, so no barrier is needed.  Registers are capped so
+// that 3 CTAs fit per SM with bf16 gradients (2 with fp32, whose reduction
+// alone needs ~120): measured on the minGPT unit, the capped kernel took
+// 12.35 ms against 13.24 ms uncapped.  Same operation sequence as the two
+// separate kernels, so the results are identical; only segment elements are
+// touched (pads stay zero, which AdamW would preserve anyway).
+template <typename GT, int NMAX, bool BF16, bool HYBRID>
+__global__ void __launch_bounds__(kBlock, sizeof(GT) == 2 ? 3 : 2) reduce_adamw_kernel(const Tile* __restrict__ tiles,
                                                               int64_t ntiles, GradPtrs<NMAX> gp,
                                                               ReduceArgs a, float* __restrict__ gshard,
                                                               float* __restrict__ p, float* __restrict__ m,
                                                               float* __restrict__ v,
                                                               uint16_t* __restrict__ shadow, AdamWConsts c) {
+    __shared__ __align__(16) float gsm[kTile];
     const int tid = threadIdx.x;
-    const float fW = static_cast<float>(a.F * a.groups);
+    const int groups = HYBRID ? a.groups : 1;
+    const float fW = static_cast<float>(a.F * groups);
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const Tile tl = tiles[t];
         const TileSplit sp = split_tile(tl.g, tl.len);
         int j = -1;
         if (tid < sp.head) j = tid;
         else if (tid >= 8 && tid < 8 + sp.tail) j = sp.head + 8 * sp.nvec + (tid - 8);
+        const int64_t g0 = tl.g + sp.head;
+        const int64_t s0 = tl.s + sp.head;
+        // phase 1: reduce
+        float xj = 0.f;
+        if (j >= 0) {
+            xj = reduce1<GT, NMAX, BF16>(gp, a, groups, fW, tl.g + j);
+            gshard[tl.s + j] = xj;
+        }
+#pragma unroll 1
+        for (int vi = tid; vi < sp.nvec; vi += kBlock) {
+            const F8 G = reduce8<GT, NMAX, BF16>(gp, a, groups, fW, g0 + 8 * static_cast<int64_t>(vi));
+            st8(gshard + s0 + 8 * static_cast<int64_t>(vi), G);
+            float4* slot = reinterpret_cast<float4*>(gsm + 8 * vi);
+            slot[0] = make_float4(G.v[0], G.v[1], G.v[2], G.v[3]);
+            slot[1] = make_float4(G.v[4], G.v[5], G.v[6], G.v[7]);
+        }
+        // phase 2: AdamW on the same elements, G from shared memory
         if (j >= 0) {
             const int64_t s = tl.s + j;
-            const float x = reduce1<GT, NMAX, BF16>(gp, a, a.groups, fW, tl.g + j);
-            gshard[s] = x;
             float pp = p[s], mm = m[s], vv = v[s];
-            adamw_elem(pp, x, mm, vv, c);
+            adamw_elem(pp, xj, mm, vv, c);
             p[s] = pp;
             m[s] = mm;
             v[s] = vv;
             shadow[s] = to_bf16(pp);
         }
-        const int64_t g0 = tl.g + sp.head;
-        const int64_t s0 = tl.s + sp.head;
+#pragma unroll 1
         for (int vi = tid; vi < sp.nvec; vi += kBlock) {
             const int64_t s = s0 + 8 * static_cast<int64_t>(vi);
             F8 P = ld8_rw(p + s);
             F8 M = ld8_rw(m + s);
             F8 V = ld8_rw(v + s);
-            const F8 G = reduce8<GT, NMAX, BF16>(gp, a, a.groups, fW, g0 + 8 * static_cast<int64_t>(vi));
-            st8(gshard + s, G);
+            const float4* slot = reinterpret_cast<const float4*>(gsm + 8 * vi);
+            const float4 lo = slot[0], hi = slot[1];
+            const float G[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) adamw_elem(P.v[e], G.v[e], M.v[e], V.v[e], c);
+            for (int e = 0; e < 8; ++e) adamw_elem(P.v[e], G[e], M.v[e], V.v[e], c);
             st8(p + s, P);
             st8(m + s, M);
             st8(v + s, V);
@@ -566,8 +589,12 @@ static cudaError_t launch_ra_t(const Tile* tiles, int64_t ntiles, const void* co
     GradPtrs<NMAX> gp;
     const int W = a.F * a.groups;
     for (int r = 0; r < NMAX; ++r) gp.p[r] = r < W ? grads[r] : nullptr;
-    reduce_adamw_kernel<GT, NMAX, BF16>
-        <<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, gp, a, gshard, p, m, v, shadow, c);
+    if (a.groups > 1)
+        reduce_adamw_kernel<GT, NMAX, BF16, true>
+            <<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, gp, a, gshard, p, m, v, shadow, c);
+    else
+        reduce_adamw_kernel<GT, NMAX, BF16, false>
+            <<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, gp, a, gshard, p, m, v, shadow, c);
     return cudaGetLastError();
 }
 

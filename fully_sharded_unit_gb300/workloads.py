@@ -183,6 +183,14 @@ def _workloads() -> dict:
         units=(gpt_block(3072, 12288, n0006, n0006, n0006),),
         N=8, layout="flat", grad_dtype="bf16", steps=2, grad_std=1e-4,
         outlier_frac=1e-3, outlier_scale=1e3)
+    for layout in ("flat", "dim0"):
+        name = f"huge_{layout}_n3"
+        w[name] = Workload(
+            name=name,
+            description=f"One unit past 2^31 elements: W[46341x46341] + b[1000] (2,147,489,281 params), "
+                        f"{layout.upper()} at N=3, bf16 grads",
+            units=((Param("w", (46341, 46341), u01), Param("b", (1000,), u01)),),
+            N=3, layout=layout, grad_dtype="bf16", steps=2, grad_std=1e-2)
     w["gpt_mini_dim0"] = Workload(
         name="gpt_mini_dim0",
         description="Reduced GPT block d=128 ffn 512 x2 units, DIM0, N=8",

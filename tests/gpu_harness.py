@@ -181,7 +181,7 @@ def _flat_window(params, offsets, idx_np: np.ndarray) -> np.ndarray:
 
 
 def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None, n_random: int = 16,
-                 seed: int = 0) -> Comparison:
+                 seed: int = 0, extra_boundaries=()) -> Comparison:
     """Full-size unit through fsdp_step (the launch configuration the bench
     times), compared on windows of global indices."""
     shapes = wl.shapes(unit)
@@ -190,7 +190,7 @@ def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None
     steps = wl.steps if steps is None else steps
     hp = workloads.hyper(wl)
     lay = O.Layout(shapes, N, wl.layout)
-    bounds = sorted({a for segs in lay.segments for a, _ in segs} | set(lay.offsets))
+    bounds = sorted({a for segs in lay.segments for a, _ in segs} | set(lay.offsets) | set(extra_boundaries))
     windows = choose_windows(P, bounds, n_random=n_random, seed=seed)
     idx = _window_index(windows)
     idx_dev = idx.cuda()

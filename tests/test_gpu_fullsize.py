@@ -50,3 +50,14 @@ def test_mingpt175b_windows_fused_shadow_gather():
     wl = workloads.get("mingpt175b_flat").with_(fuse_reduce_adamw=True, gather_source="shadow")
     cmp = H.run_windowed(wl, unit=0)
     assert cmp.covered > 1_000_000
+
+
+@pytest.mark.parametrize("name", ["huge_flat_n3", "huge_dim0_n3"])
+def test_unit_past_2_31_elements(name):
+    """P = 2,147,489,281 > 2^31: offsets, tiles and slab indices are 64-bit;
+    windows cover every shard boundary and the 2^31 element boundary."""
+    wl = workloads.get(name)
+    assert wl.unit_numel(0) > 2 ** 31
+    cmp = H.run_windowed(wl, extra_boundaries=(2 ** 31, 2 ** 31 - 8192))
+    assert cmp.covered > 1_000_000
+    torch.cuda.empty_cache()
