@@ -248,7 +248,8 @@ def selected_workload(args) -> workloads.Workload:
     wl = workloads.get(args.workload)
     over = {k: v for k, v in (("gather_source", args.gather_source), ("layout", args.layout),
                               ("reduce_dtype", args.reduce_dtype),
-                              ("fuse_reduce_adamw", None if args.fuse is None else args.fuse == "on"))
+                              ("fuse_reduce_adamw", None if args.fuse is None else args.fuse == "on"),
+                              ("replicas", args.replicas))
             if v is not None}
     return wl.with_(**over) if over else wl
 
@@ -282,13 +283,29 @@ def run_ours(args, world, rank, local):
         workloads.grad_tensor(wl, 0, 0, r, dev, out=grads[r][:units[0].numel])
     out = torch.empty(P_max, dtype=torch.int16, device=dev)
     cb = [counted_bytes(wl, i) for i in range(wl.n_units)]
+    if args.micro_batches > 1:
+        assert not wl.fuse_reduce_adamw, "micro-batches use the separate reduce-scatter and AdamW"
+        for i, c in enumerate(cb):
+            acc = c["reduce_scatter"] + 4 * wl.unit_numel(i)      # also reads the shard it adds to
+            c["step"] += (args.micro_batches - 1) * acc
+            c["reduce_scatter"] = (c["reduce_scatter"] + (args.micro_batches - 1) * acc) / args.micro_batches
     step_bytes = sum(c["step"] for c in cb)
     stream = torch.cuda.current_stream()
+
+    K = args.micro_batches
 
     def step():
         for i, u in enumerate(units):
             g = grads if units[i].numel == P_max else [x[:u.numel] for x in grads]
-            u.step(g, out, hp, stream)
+            if K == 1:
+                u.step(g, out, hp, stream)
+                continue
+            u.allgather(out, stream)
+            if wl.reshard_after_forward:
+                u.allgather(out, stream)
+            for k in range(K):
+                u.reduce_scatter_ex(g, accumulate=k > 0, stream=stream)
+            u.adamw_step(hp, stream)
 
     for _ in range(args.warmup):
         step()
@@ -324,7 +341,9 @@ def run_ours(args, world, rank, local):
         launches += n
     dom = max(per_kernel, key=lambda k: per_kernel[k][0])
     dom_ms, dom_n = per_kernel[dom]
-    dom_bytes = sum(c[dom] * (c["gathers"] if dom == "gather" else 1) for c in cb) / \
+    per_step = {"gather": lambda c: c["gather"] * c["gathers"],
+                "reduce_scatter": lambda c: c["reduce_scatter"] * args.micro_batches}
+    dom_bytes = sum(per_step.get(dom, lambda c: c[dom])(c) for c in cb) / \
         (dom_n / args.steps)      # counted bytes per launch
     achieved = dom_bytes / (dom_ms / dom_n * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
@@ -332,7 +351,7 @@ def run_ours(args, world, rank, local):
                 "frac": achieved / peak, "peak_source": peak_kind,
                 "traffic": recorded_traffic(dom, wl.name),
                 "per_kernel_ms_per_launch": {k: (v[0] / v[1] if v[1] else None) for k, v in per_kernel.items()},
-                "per_kernel_gbs": {k: (sum(c[k] * (c["gathers"] if k == "gather" else 1) for c in cb) /
+                "per_kernel_gbs": {k: (sum(per_step.get(k, lambda c: c[k])(c) for c in cb) /
                                        (v[1] / args.steps) / (v[0] / v[1] * 1e-3) / 1e9 if v[1] else None)
                                    for k, v in per_kernel.items()}}
 
@@ -341,7 +360,7 @@ def run_ours(args, world, rank, local):
 
     # end to end through the public API with host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.micro_batches == 1:
         e2e = run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world)
 
     cpu = None
@@ -365,7 +384,7 @@ def run_ours(args, world, rank, local):
                    "layout": wl.layout, "grad_dtype": wl.grad_dtype,
                    "reshard_after_forward": wl.reshard_after_forward,
                    "replicas": wl.replicas, "reduce_dtype": wl.reduce_dtype,
-                   "fused_reduce_adamw": wl.fuse_reduce_adamw,
+                   "fused_reduce_adamw": wl.fuse_reduce_adamw, "micro_batches": args.micro_batches,
                    "counted_bytes_per_step": step_bytes,
                    "gather_source": "fp32 master" if wl.gather_source == "master" else "bf16 shadow",
                    "l2": "inputs larger than L2; no flush", "parallelism": f"replicas x{world}"},
@@ -458,6 +477,11 @@ def main(argv=None):
                     help="override the workload's gather source")
     ap.add_argument("--layout", choices=["flat", "dim0", "flat_padded"], default=None)
     ap.add_argument("--reduce-dtype", choices=["f32", "bf16"], default=None)
+    ap.add_argument("--replicas", type=int, default=None,
+                    help="hybrid sharding: replication groups (the workload's N ranks per group)")
+    ap.add_argument("--micro-batches", type=int, default=1,
+                    help="gradient accumulation: reduce-scatters per step (the first overwrites, "
+                         "the rest accumulate), then one AdamW")
     ap.add_argument("--fuse", choices=["on", "off"], default=None,
                     help="override whether fsdp_step fuses reduce-scatter and AdamW")
     args = ap.parse_args(argv)
