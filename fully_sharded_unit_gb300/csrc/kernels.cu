@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "kernels.hpp"
 
@@ -265,8 +266,15 @@ __device__ __forceinline__ float reduce1(const GradPtrs<NMAX>& gp, const ReduceA
                                          float fW, int64_t i) {
     using IO = GradIO<GT>;
     if (BF16) {
-        float acc = round_bf16(IO::load1(gp.p[0], i));
-        for (int r = 1; r < a.F; ++r) acc = round_bf16(__fadd_rn(acc, round_bf16(IO::load1(gp.p[r], i))));
+        // bf16 gradients are already bf16; only fp32 inputs need the rounding
+        constexpr bool round_in = !std::is_same<GT, uint16_t>::value;
+        float acc = IO::load1(gp.p[0], i);
+        if (round_in) acc = round_bf16(acc);
+        for (int r = 1; r < a.F; ++r) {
+            float x = IO::load1(gp.p[r], i);
+            if (round_in) x = round_bf16(x);
+            acc = round_bf16(__fadd_rn(acc, x));
+        }
         return round_bf16(__fdiv_rn(acc, fW));
     }
     float tot = 0.f;
@@ -298,7 +306,7 @@ __device__ __forceinline__ F8 reduce8(const GradPtrs<NMAX>& gp, const ReduceArgs
                 if (r0 + b < a.F) {
                     F8 w;
                     IO::widen(x[b], w);
-                    if (BF16) {
+                    if (BF16 && !std::is_same<GT, uint16_t>::value) {   // bf16 inputs are exact
 #pragma unroll
                         for (int e = 0; e < 8; ++e) w.v[e] = round_bf16(w.v[e]);
                     }
