@@ -81,7 +81,6 @@ struct fsdp_unit {
     Tile* load_tiles = nullptr;
     int64_t nload_tiles = 0;
     fsdp::ParamSrc* param_src = nullptr;
-    int sms = 1;
     int64_t t = 0;
     bool loaded = false;
     bool profiling = false;
@@ -197,8 +196,8 @@ fsdp::AdamWConsts adamw_consts(const fsdp_adamw_hp* hp, int64_t t) {
 int enqueue_gather(fsdp_unit* u, uint16_t* out, cudaStream_t st) {
     return profiled_launch(u, FSDP_KERNEL_GATHER, st, "gather launch", [&] {
         if (u->gather_source == FSDP_GATHER_FROM_SHADOW)
-            return fsdp::launch_gather_shadow(u->tiles, u->ntiles, u->shadow, out, u->sms, st);
-        return fsdp::launch_gather(u->tiles, u->ntiles, u->master, out, u->sms, st);
+            return fsdp::launch_gather_shadow(u->tiles, u->ntiles, u->shadow, out, st);
+        return fsdp::launch_gather(u->tiles, u->ntiles, u->master, out, st);
     });
 }
 
@@ -231,8 +230,7 @@ int enqueue_reduce_scatter(fsdp_unit* u, const void* const* grads, const fsdp_rs
         }
     }
     return profiled_launch(u, FSDP_KERNEL_REDUCE_SCATTER, st, "reduce-scatter launch", [&] {
-        return fsdp::launch_reduce_scatter(u->tiles, u->ntiles, grads, u->grad_dtype, a, u->grad,
-                                           u->sms, st);
+        return fsdp::launch_reduce_scatter(u->tiles, u->ntiles, grads, u->grad_dtype, a, u->grad, st);
     });
 }
 
@@ -255,8 +253,7 @@ int enqueue_reduce_adamw(fsdp_unit* u, const void* const* grads, const fsdp_adam
 int enqueue_adamw(fsdp_unit* u, const fsdp_adamw_hp* hp, cudaStream_t st) {
     const fsdp::AdamWConsts c = adamw_consts(hp, u->t + 1);
     int rc = profiled_launch(u, FSDP_KERNEL_ADAMW, st, "AdamW launch", [&] {
-        return fsdp::launch_adamw(u->plan.slab_len / 8, u->master, u->grad, u->m, u->v, u->shadow, c,
-                                  u->sms, st);
+        return fsdp::launch_adamw(u->plan.slab_len / 8, u->master, u->grad, u->m, u->v, u->shadow, c, st);
     });
     if (rc == FSDP_OK) u->t += 1;
     return rc;
@@ -388,7 +385,6 @@ int fsdp_unit_create(int nparams, const int* ndims, const int64_t* dims,
     if (e == cudaSuccess && !load_tiles.empty())
         e = cudaMemcpy(u->load_tiles, load_tiles.data(), load_tiles.size() * sizeof(Tile),
                        cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = fsdp::device_sms(u->device, &u->sms);
     if (e != cudaSuccess) {
         free_unit(u);
         delete u;
@@ -434,8 +430,7 @@ int fsdp_load_params(fsdp_unit* u, const float* const* params, void* stream) {
     if (e == cudaSuccess) e = cudaMemsetAsync(u->shadow, 0, S * 2, st);
     if (e != cudaSuccess) return cuda_fail(e, "load set-up");
     rc = profiled_launch(u, FSDP_KERNEL_SHARD_IN, st, "shard-in launch", [&] {
-        return fsdp::launch_shard_in(u->load_tiles, u->nload_tiles, u->param_src, u->master, u->shadow,
-                                     u->sms, st);
+        return fsdp::launch_shard_in(u->load_tiles, u->nload_tiles, u->param_src, u->master, u->shadow, st);
     });
     if (rc) return rc;
     u->t = 0;
@@ -523,8 +518,7 @@ static int copy_state(const fsdp_unit* u, int which, int rank, void* ext, bool t
         if (e != cudaSuccess) return cuda_fail(e, "state copy");
     }
     if (to_unit && which == FSDP_STATE_PARAM) {   // keep shadow == RNE(master)
-        cudaError_t e = fsdp::launch_cast_range(u->master, u->shadow, abase, u->plan.arena_len[rank],
-                                                u->sms, st);
+        cudaError_t e = fsdp::launch_cast_range(u->master, u->shadow, abase, u->plan.arena_len[rank], st);
         if (e != cudaSuccess) return cuda_fail(e, "shadow refresh");
     }
     return FSDP_OK;

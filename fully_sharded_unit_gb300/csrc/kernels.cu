@@ -513,39 +513,29 @@ unsigned grid_for(int64_t work) {
 
 }  // namespace
 
-cudaError_t device_sms(int device, int* sms) {
-    return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, device);
-}
-
 cudaError_t launch_shard_in(const Tile* tiles, int64_t ntiles, const ParamSrc* params,
-                            float* master, uint16_t* shadow, int sms, cudaStream_t st) {
+                            float* master, uint16_t* shadow, cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
-    (void)sms;
     shard_in_kernel<<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, params, master, shadow);
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const Tile* tiles, int64_t ntiles, const float* master, uint16_t* out,
-                          int sms, cudaStream_t st) {
+cudaError_t launch_gather(const Tile* tiles, int64_t ntiles, const float* master, uint16_t* out, cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
-    (void)sms;
     gather_cast_kernel<<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, master, out);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather_shadow(const Tile* tiles, int64_t ntiles, const uint16_t* shadow,
-                                 uint16_t* out, int sms, cudaStream_t st) {
+                                 uint16_t* out, cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
-    (void)sms;
     gather_shadow_kernel<<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, shadow, out);
     return cudaGetLastError();
 }
 
-cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t begin, int64_t n,
-                              int sms, cudaStream_t st) {
+cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t begin, int64_t n, cudaStream_t st) {
     const int64_t n8 = n / 8;
     if (n8 == 0) return cudaSuccess;
-    (void)sms;
     cast_range_kernel<<<grid_for((n8 + kBlock - 1) / kBlock), kBlock, 0, st>>>(
         master + begin, shadow + begin, n8);
     return cudaGetLastError();
@@ -553,8 +543,7 @@ cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t beg
 
 template <typename GT, int NMAX, bool BF16, bool EXT>
 static cudaError_t launch_rs_t(const Tile* tiles, int64_t ntiles, const void* const* grads,
-                               const ReduceArgs& a, float* gshard, int sms, cudaStream_t st) {
-    (void)sms;
+                               const ReduceArgs& a, float* gshard, cudaStream_t st) {
     GradPtrs<NMAX> gp;
     const int W = a.F * a.groups;
     for (int r = 0; r < NMAX; ++r) gp.p[r] = r < W ? grads[r] : nullptr;
@@ -565,29 +554,28 @@ static cudaError_t launch_rs_t(const Tile* tiles, int64_t ntiles, const void* co
 
 template <typename GT, int NMAX, bool BF16>
 static cudaError_t launch_rs_ext(const Tile* tiles, int64_t ntiles, const void* const* grads,
-                                 const ReduceArgs& a, float* gshard, int sms, cudaStream_t st) {
+                                 const ReduceArgs& a, float* gshard, cudaStream_t st) {
     const bool ext = a.groups > 1 || a.scale || a.accumulate || a.found != nullptr;
-    return ext ? launch_rs_t<GT, NMAX, BF16, true>(tiles, ntiles, grads, a, gshard, sms, st)
-               : launch_rs_t<GT, NMAX, BF16, false>(tiles, ntiles, grads, a, gshard, sms, st);
+    return ext ? launch_rs_t<GT, NMAX, BF16, true>(tiles, ntiles, grads, a, gshard, st)
+               : launch_rs_t<GT, NMAX, BF16, false>(tiles, ntiles, grads, a, gshard, st);
 }
 
 template <typename GT>
 static cudaError_t launch_rs_dt(const Tile* tiles, int64_t ntiles, const void* const* grads,
-                                const ReduceArgs& a, float* gshard, int sms, cudaStream_t st) {
+                                const ReduceArgs& a, float* gshard, cudaStream_t st) {
     const bool small = a.F * a.groups <= 64;
     if (a.bf16_reduce)
-        return small ? launch_rs_ext<GT, 64, true>(tiles, ntiles, grads, a, gshard, sms, st)
-                     : launch_rs_ext<GT, kMaxRanks, true>(tiles, ntiles, grads, a, gshard, sms, st);
-    return small ? launch_rs_ext<GT, 64, false>(tiles, ntiles, grads, a, gshard, sms, st)
-                 : launch_rs_ext<GT, kMaxRanks, false>(tiles, ntiles, grads, a, gshard, sms, st);
+        return small ? launch_rs_ext<GT, 64, true>(tiles, ntiles, grads, a, gshard, st)
+                     : launch_rs_ext<GT, kMaxRanks, true>(tiles, ntiles, grads, a, gshard, st);
+    return small ? launch_rs_ext<GT, 64, false>(tiles, ntiles, grads, a, gshard, st)
+                 : launch_rs_ext<GT, kMaxRanks, false>(tiles, ntiles, grads, a, gshard, st);
 }
 
 cudaError_t launch_reduce_scatter(const Tile* tiles, int64_t ntiles, const void* const* grads,
-                                  int grad_dtype, const ReduceArgs& a, float* gshard, int sms,
-                                  cudaStream_t st) {
+                                  int grad_dtype, const ReduceArgs& a, float* gshard, cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
-    if (grad_dtype == FSDP_DTYPE_BF16) return launch_rs_dt<uint16_t>(tiles, ntiles, grads, a, gshard, sms, st);
-    return launch_rs_dt<float>(tiles, ntiles, grads, a, gshard, sms, st);
+    if (grad_dtype == FSDP_DTYPE_BF16) return launch_rs_dt<uint16_t>(tiles, ntiles, grads, a, gshard, st);
+    return launch_rs_dt<float>(tiles, ntiles, grads, a, gshard, st);
 }
 
 template <typename GT, int NMAX, bool BF16>
@@ -628,9 +616,8 @@ cudaError_t launch_reduce_adamw(const Tile* tiles, int64_t ntiles, const void* c
 }
 
 cudaError_t launch_adamw(int64_t n8, float* p, const float* g, float* m, float* v,
-                         uint16_t* shadow, const AdamWConsts& c, int sms, cudaStream_t st) {
+                         uint16_t* shadow, const AdamWConsts& c, cudaStream_t st) {
     if (n8 == 0) return cudaSuccess;
-    (void)sms;
     adamw_kernel<<<grid_for((n8 + kBlock - 1) / kBlock), kBlock, 0, st>>>(n8, p, g, m, v, shadow, c);
     return cudaGetLastError();
 }

@@ -36,30 +36,24 @@ struct ReduceArgs {
     int32_t* found;     // set to 1 when a written value is not finite; may be null
 };
 
-// Number of SMs of the unit's device (kept for launch policies that size
-// grids by the SM count; the current kernels launch one CTA per unit of work).
-cudaError_t device_sms(int device, int* sms);
-
 cudaError_t launch_shard_in(const Tile* tiles, int64_t ntiles, const ParamSrc* params,
-                            float* master, uint16_t* shadow, int sms, cudaStream_t st);
+                            float* master, uint16_t* shadow, cudaStream_t st);
 
 cudaError_t launch_gather(const Tile* tiles, int64_t ntiles, const float* master,
-                          uint16_t* out, int sms, cudaStream_t st);
+                          uint16_t* out, cudaStream_t st);
 
 // The gather from the bf16 shadow shards (a copy; the cast was done by AdamW
 // or shard-in).
 cudaError_t launch_gather_shadow(const Tile* tiles, int64_t ntiles, const uint16_t* shadow,
-                                 uint16_t* out, int sms, cudaStream_t st);
+                                 uint16_t* out, cudaStream_t st);
 
 // grads: W = a.F * a.groups pointers (fp32 or bf16 per grad_dtype), each P elements.
 cudaError_t launch_reduce_scatter(const Tile* tiles, int64_t ntiles, const void* const* grads,
-                                  int grad_dtype, const ReduceArgs& a, float* gshard, int sms,
-                                  cudaStream_t st);
+                                  int grad_dtype, const ReduceArgs& a, float* gshard, cudaStream_t st);
 
 // shadow[i] = RNE_bf16(master[i]) for i in [begin, begin + n); begin and n
 // multiples of 8.
-cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t begin, int64_t n,
-                              int sms, cudaStream_t st);
+cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t begin, int64_t n, cudaStream_t st);
 
 // Fused reduce-scatter (no unscale / accumulation / flag) and AdamW over the
 // unit's segments; a.F * a.groups gradient pointers.
@@ -69,6 +63,6 @@ cudaError_t launch_reduce_adamw(const Tile* tiles, int64_t ntiles, const void* c
 
 // n8: number of 8-element groups in the slab (slab length / 8).
 cudaError_t launch_adamw(int64_t n8, float* p, const float* g, float* m, float* v,
-                         uint16_t* shadow, const AdamWConsts& c, int sms, cudaStream_t st);
+                         uint16_t* shadow, const AdamWConsts& c, cudaStream_t st);
 
 }  // namespace fsdp
