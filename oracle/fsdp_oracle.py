@@ -488,20 +488,23 @@ class UnitOracle:
 # Element windows (for units too large to hold on the host)
 # --------------------------------------------------------------------------
 
-def run_window(params_window, grads_windows_per_step, hp: AdamWHyper):
+def run_window(params_window, grads_windows_per_step, hp: AdamWHyper, reduce=None):
     """The cycle restricted to a window of global indices.  Every operation
     after the layout is elementwise in the global index, so the master, m, v,
     gradient shard and gathered values at index i depend only on the initial
-    parameter at i and the N ranks' gradients at i.  Returns, per step, the
-    (gathered bf16, reduced fp32 gradient) of the window and the final
-    (master, m, v)."""
+    parameter at i and the ranks' gradients at i.  ``reduce`` maps the list of
+    gradient windows to the reduced gradient (default: the plain rank-order
+    fold, ``reduce_full``; also ``reduce_full_bf16`` or a hybrid fold).
+    Returns, per step, the (gathered bf16, reduced fp32 gradient) of the
+    window and the final (master, m, v)."""
+    reduce = reduce_full if reduce is None else reduce
     p = np.asarray(params_window, F32).copy()
     m = np.zeros_like(p)
     v = np.zeros_like(p)
     per_step = []
     for t, grads in enumerate(grads_windows_per_step, start=1):
         gathered = bf16_rne(p)
-        G = reduce_full(grads)
+        G = reduce(grads)
         p, m, v = adamw_update(p, G, m, v, t, hp)
         per_step.append((gathered, G))
     return per_step, (p, m, v)

@@ -186,7 +186,6 @@ def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None
     times), compared on windows of global indices."""
     shapes = wl.shapes(unit)
     N, P = wl.N, wl.unit_numel(unit)
-    assert wl.replicas == 1 and wl.reduce_dtype == "f32", "windows use the plain fp32 reduction"
     steps = wl.steps if steps is None else steps
     hp = workloads.hyper(wl)
     lay = O.Layout(shapes, N, wl.layout)
@@ -195,19 +194,20 @@ def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None
     idx = _window_index(windows)
     idx_dev = idx.cuda()
     cmp = Comparison()
-    u = B.Unit(shapes, wl.layout, N, wl.grad_dtype, wl.reshard_after_forward,
-               gather_source=wl.gather_source, fuse_reduce_adamw=wl.fuse_reduce_adamw)
+    u = B.Unit(shapes, wl.layout, N, wl.grad_dtype, wl.reshard_after_forward, replicas=wl.replicas,
+               reduce_dtype=wl.reduce_dtype, gather_source=wl.gather_source,
+               fuse_reduce_adamw=wl.fuse_reduce_adamw)
     try:
         params = workloads.param_tensors(wl, unit, "cuda")
         p_win = _flat_window(params, lay.offsets, idx.numpy())
         u.load(params)
         torch.cuda.synchronize()
         del params
-        gdev = [torch.empty(P, dtype=wl.torch_grad_dtype(), device="cuda") for _ in range(N)]
+        gdev = [torch.empty(P, dtype=wl.torch_grad_dtype(), device="cuda") for _ in range(wl.world)]
         out = torch.empty(P, dtype=torch.int16, device="cuda")
         g_win, out_win, gs_win = [], [], []
         for s in range(steps):
-            for r in range(N):
+            for r in range(wl.world):
                 workloads.grad_tensor(wl, unit, s, r, "cuda", out=gdev[r])
             g_win.append([grad_np(g[idx_dev]) for g in gdev])
             u.step(gdev, out, hp)
@@ -220,7 +220,14 @@ def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None
         del gdev, out
     finally:
         u.close()
-    per_step, (p, m, v) = O.run_window(p_win, g_win, O.AdamWHyper(**hp))
+    if wl.replicas > 1:
+        def reduce(gs):
+            return O.reduce_full_hybrid(gs, N)
+    elif wl.reduce_dtype == "bf16":
+        reduce = O.reduce_full_bf16
+    else:
+        reduce = O.reduce_full
+    per_step, (p, m, v) = O.run_window(p_win, g_win, O.AdamWHyper(**hp), reduce=reduce)
     for s, (gathered, G) in enumerate(per_step):
         assert_bits_equal(out_win[s], gathered, f"step {s} gathered (windows)")
         assert_bits_equal(gs_win[s], G, f"step {s} grad shard (windows)")

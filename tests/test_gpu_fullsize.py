@@ -61,3 +61,18 @@ def test_unit_past_2_31_elements(name):
     cmp = H.run_windowed(wl, extra_boundaries=(2 ** 31, 2 ** 31 - 8192))
     assert cmp.covered > 1_000_000
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("kw", [
+    dict(replicas=2),                                   # hybrid: 2 sharding groups of 8, W = 16 gradients
+    dict(reduce_dtype="bf16"),                          # reductions in bf16
+    dict(layout="flat_padded", gather_source="shadow"),  # the paper's padded FlatParameter, bf16 gather
+    dict(layout="dim0", fuse_reduce_adamw=True, replicas=2),
+])
+def test_mingpt175b_next_rows_windows(kw):
+    """The rows beyond the basic cycle at the full minGPT-175B unit size,
+    through fsdp_step, compared on windows."""
+    wl = workloads.get("mingpt175b_flat").with_(**kw)
+    cmp = H.run_windowed(wl, unit=0)
+    assert cmp.covered > 1_000_000
+    torch.cuda.empty_cache()

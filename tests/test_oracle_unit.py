@@ -161,3 +161,29 @@ def test_memory_examples_printed_on_pages():
     u = O.UnitOracle([(psi,)], N, "flat")
     d = u.memory_bytes(0)
     assert abs((d["param"] + d["adam"]) / 2**30 - float(fsdp_gib)) < 0.005
+
+
+@pytest.mark.parametrize("replicas,reduce_dtype", [(2, "f32"), (3, "f32"), (1, "bf16")])
+def test_window_run_equals_unit_run_for_hybrid_and_bf16(replicas, reduce_dtype):
+    rng = np.random.default_rng(5)
+    shapes = [(40, 11), (11,)]
+    params = [rng.normal(0, 0.02, s).astype(np.float32) for s in shapes]
+    N, P = 3, 451
+    W = N * replicas
+    grads = [[rng.normal(0, 1e-3, P).astype(np.float32) for _ in range(W)] for _ in range(3)]
+    hp = O.AdamWHyper()
+    u = O.UnitOracle(shapes, N, "flat", hp, replicas=replicas, reduce_dtype=reduce_dtype)
+    u.load(params)
+    outs = [u.step(g) for g in grads]
+    if replicas > 1:
+        def reduce(gs):
+            return O.reduce_full_hybrid(gs, N)
+    else:
+        reduce = O.reduce_full_bf16
+    a, b = 50, 400
+    per_step, (p, m, v) = O.run_window(O.flatten(params)[a:b], [[g[a:b] for g in gs] for gs in grads], hp,
+                                       reduce=reduce)
+    for s, (gathered, G) in enumerate(per_step):
+        assert np.array_equal(gathered, outs[s][0][a:b])
+    assert np.array_equal(p, u.full("master")[a:b])
+    assert np.array_equal(v, u.full("v")[a:b])
