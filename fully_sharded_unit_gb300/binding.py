@@ -105,6 +105,7 @@ _SIGNATURES = {
     "fsdp_get_state": (_I, [_P, _I, _I, _P, _P]),
     "fsdp_set_state": (_I, [_P, _I, _I, _P, _P]),
     "fsdp_read_global": (_I, [_P, _I, _I64, _I64, _P, _P]),
+    "fsdp_read_arena": (_I, [_P, _I, _I, _P, _PI64, _P]),
     "fsdp_get_step_count": (_I, [_P, _PI64]),
     "fsdp_set_step_count": (_I, [_P, _I64]),
     "fsdp_unit_info": (_I, [_P, _PI64, ctypes.POINTER(UnitConfig)]),
@@ -298,6 +299,18 @@ def fsdp_read_global(h, which, begin, count, dst: torch.Tensor, stream=None) -> 
     assert dst.numel() >= count
     _check(lib().fsdp_read_global(h, which, int(begin), int(count), dst.data_ptr(), _stream(stream)),
            "fsdp_read_global")
+
+
+def fsdp_read_arena(h, which, rank, stream=None) -> torch.Tensor:
+    """Rank ``rank``'s whole arena of state ``which`` (pads included), on the device."""
+    which = STATES.get(which, which)
+    n = ctypes.c_int64()
+    _check(lib().fsdp_read_arena(h, which, rank, None, ctypes.byref(n), _stream(stream)), "fsdp_read_arena")
+    dt = torch.int16 if which == FSDP_STATE_SHADOW else torch.float32
+    dst = torch.empty(n.value, dtype=dt, device="cuda")
+    if n.value:
+        _check(lib().fsdp_read_arena(h, which, rank, dst.data_ptr(), None, _stream(stream)), "fsdp_read_arena")
+    return dst
 
 
 def fsdp_get_step_count(h) -> int:

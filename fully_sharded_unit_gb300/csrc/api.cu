@@ -558,6 +558,23 @@ int fsdp_read_global(const fsdp_unit* u, int which, int64_t begin, int64_t count
     return FSDP_OK;
 }
 
+int fsdp_read_arena(const fsdp_unit* u, int which, int rank, void* dst, int64_t* arena_len, void* stream) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    if (rank < 0 || rank >= u->plan.N) return fail(FSDP_E_INVALID_ARG, "rank out of range");
+    size_t esz = 0;
+    char* base = state_base(u, which, &esz);
+    if (base == nullptr) return fail(FSDP_E_INVALID_ARG, "unknown state");
+    const int64_t n = u->plan.arena_len[rank];
+    if (arena_len) *arena_len = n;
+    if (dst == nullptr) return FSDP_OK;   // size query
+    DeviceGuard dg(u->device);
+    cudaError_t e = cudaMemcpyAsync(dst, base + static_cast<size_t>(u->plan.arena_base[rank]) * esz,
+                                    static_cast<size_t>(n) * esz, cudaMemcpyDefault,
+                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "arena copy");
+}
+
 int fsdp_get_step_count(const fsdp_unit* u, int64_t* t) {
     int rc = check_unit(u, false);
     if (rc) return rc;

@@ -263,6 +263,15 @@ FSDP_API int fsdp_set_state(fsdp_unit* unit, int which, int rank, const void* sr
 FSDP_API int fsdp_read_global(const fsdp_unit* unit, int which, int64_t begin, int64_t count,
                      void* dst, void* stream);
 
+/* Copy rank `rank`'s whole device arena of state `which`, alignment pads and
+ * layout padding included (arena_len elements, see fsdp_memory_report /
+ * fsdp_segment.arena_off), to `dst`; with dst NULL only *arena_len is set.
+ * For integrity checks: every element
+ * outside the rank's segments is zero from creation and must stay zero; a
+ * non-zero pad means some kernel wrote outside its segment. */
+FSDP_API int fsdp_read_arena(const fsdp_unit* unit, int which, int rank, void* dst, int64_t* arena_len,
+                             void* stream);
+
 /* AdamW step count t (0 after load). */
 FSDP_API int fsdp_get_step_count(const fsdp_unit* unit, int64_t* t);
 FSDP_API int fsdp_set_step_count(fsdp_unit* unit, int64_t t);
