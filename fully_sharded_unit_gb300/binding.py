@@ -106,6 +106,8 @@ _SIGNATURES = {
     "fsdp_set_state": (_I, [_P, _I, _I, _P, _P]),
     "fsdp_read_global": (_I, [_P, _I, _I64, _I64, _P, _P]),
     "fsdp_read_arena": (_I, [_P, _I, _I, _P, _PI64, _P]),
+    "fsdp_adamw_device_steps": (_I, [_P, ctypes.POINTER(AdamWHp), _I64, _P]),
+    "fsdp_adamw_device_status": (_I, [_P, _PI64, ctypes.POINTER(ctypes.c_int32), _P]),
     "fsdp_get_step_count": (_I, [_P, _PI64]),
     "fsdp_set_step_count": (_I, [_P, _I64]),
     "fsdp_unit_info": (_I, [_P, _PI64, ctypes.POINTER(UnitConfig)]),
@@ -311,6 +313,20 @@ def fsdp_read_arena(h, which, rank, stream=None) -> torch.Tensor:
     if n.value:
         _check(lib().fsdp_read_arena(h, which, rank, dst.data_ptr(), None, _stream(stream)), "fsdp_read_arena")
     return dst
+
+
+def fsdp_adamw_device_steps(h, hp, count, stream=None) -> None:
+    hpv = _hp(hp) if hp is not None else None
+    _check(lib().fsdp_adamw_device_steps(h, ctypes.byref(hpv) if hpv is not None else None, int(count),
+                                         _stream(stream)), "fsdp_adamw_device_steps")
+
+
+def fsdp_adamw_device_status(h, stream=None):
+    t = ctypes.c_int64()
+    ex = ctypes.c_int32()
+    _check(lib().fsdp_adamw_device_status(h, ctypes.byref(t), ctypes.byref(ex), _stream(stream)),
+           "fsdp_adamw_device_status")
+    return t.value, bool(ex.value)
 
 
 def fsdp_get_step_count(h) -> int:

@@ -71,6 +71,16 @@ struct fsdp_unit {
     int reduce_dtype = FSDP_DTYPE_F32;
     int gather_source = FSDP_GATHER_FROM_MASTER;
     int fuse = 0;
+    // device-step mode (CUDA-graph replay of AdamW): constants of steps
+    // step_base+1 .. step_base+step_count live in step_table; step_counter
+    // counts the steps taken on the device since the table was made
+    bool device_steps = false;
+    fsdp::AdamWConsts* step_table = nullptr;
+    int64_t step_table_cap = 0;
+    int64_t step_count = 0;
+    int64_t step_base = 0;
+    int64_t* step_counter = nullptr;
+    int32_t* step_status = nullptr;
     float* master = nullptr;
     float* grad = nullptr;
     float* m = nullptr;
@@ -93,7 +103,9 @@ void free_unit(fsdp_unit* u) {
     for (void* p : {static_cast<void*>(u->master), static_cast<void*>(u->grad),
                     static_cast<void*>(u->m), static_cast<void*>(u->v),
                     static_cast<void*>(u->shadow), static_cast<void*>(u->tiles),
-                    static_cast<void*>(u->load_tiles), static_cast<void*>(u->param_src)}) {
+                    static_cast<void*>(u->load_tiles), static_cast<void*>(u->param_src),
+                    static_cast<void*>(u->step_table), static_cast<void*>(u->step_counter),
+                    static_cast<void*>(u->step_status)}) {
         if (p) cudaFree(p);
     }
     for (auto& r : u->prof) {
@@ -193,6 +205,26 @@ fsdp::AdamWConsts adamw_consts(const fsdp_adamw_hp* hp, int64_t t) {
     return c;
 }
 
+fsdp::StepSource step_source(const fsdp_unit* u, const fsdp_adamw_hp* hp) {
+    fsdp::StepSource s{};
+    if (u->device_steps) {
+        s.table = u->step_table;
+        s.counter = u->step_counter;
+        s.count = u->step_count;
+        s.status = u->step_status;
+    } else {
+        s.c = adamw_consts(hp, u->t + 1);
+    }
+    return s;
+}
+
+// After an AdamW launch in device-step mode: advance the device counter.
+int advance_device_step(fsdp_unit* u, cudaStream_t st) {
+    if (!u->device_steps) return FSDP_OK;
+    cudaError_t e = fsdp::launch_advance_step(u->step_counter, u->step_count, st);
+    return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "step-counter launch");
+}
+
 int enqueue_gather(fsdp_unit* u, uint16_t* out, cudaStream_t st) {
     return profiled_launch(u, FSDP_KERNEL_GATHER, st, "gather launch", [&] {
         if (u->gather_source == FSDP_GATHER_FROM_SHADOW)
@@ -241,20 +273,22 @@ int enqueue_reduce_adamw(fsdp_unit* u, const void* const* grads, const fsdp_adam
     a.groups = u->replicas;
     a.bf16_reduce = u->reduce_dtype == FSDP_DTYPE_BF16 ? 1 : 0;
     a.inv_scale = 1.0f;
-    const fsdp::AdamWConsts c = adamw_consts(hp, u->t + 1);
+    const fsdp::StepSource c = step_source(u, hp);
     int rc = profiled_launch(u, FSDP_KERNEL_REDUCE_ADAMW, st, "fused reduce-scatter + AdamW launch", [&] {
         return fsdp::launch_reduce_adamw(u->tiles, u->ntiles, grads, u->grad_dtype, a, u->grad, u->master,
                                          u->m, u->v, u->shadow, c, st);
     });
+    if (rc == FSDP_OK) rc = advance_device_step(u, st);
     if (rc == FSDP_OK) u->t += 1;
     return rc;
 }
 
 int enqueue_adamw(fsdp_unit* u, const fsdp_adamw_hp* hp, cudaStream_t st) {
-    const fsdp::AdamWConsts c = adamw_consts(hp, u->t + 1);
+    const fsdp::StepSource c = step_source(u, hp);
     int rc = profiled_launch(u, FSDP_KERNEL_ADAMW, st, "AdamW launch", [&] {
         return fsdp::launch_adamw(u->plan.slab_len / 8, u->master, u->grad, u->m, u->v, u->shadow, c, st);
     });
+    if (rc == FSDP_OK) rc = advance_device_step(u, st);
     if (rc == FSDP_OK) u->t += 1;
     return rc;
 }
@@ -434,6 +468,7 @@ int fsdp_load_params(fsdp_unit* u, const float* const* params, void* stream) {
     });
     if (rc) return rc;
     u->t = 0;
+    u->device_steps = false;
     u->loaded = true;
     return FSDP_OK;
 }
@@ -587,7 +622,83 @@ int fsdp_set_step_count(fsdp_unit* u, int64_t t) {
     int rc = check_unit(u, false);
     if (rc) return rc;
     if (t < 0) return fail(FSDP_E_INVALID_ARG, "step count must be >= 0");
+    if (u->device_steps) return fail(FSDP_E_STATE, "device-step mode is on; turn it off first");
     u->t = t;
+    return FSDP_OK;
+}
+
+int fsdp_adamw_device_steps(fsdp_unit* u, const fsdp_adamw_hp* hp, int64_t count, void* stream) {
+    int rc = check_unit(u, true);
+    if (rc) return rc;
+    if (count < 0) return fail(FSDP_E_INVALID_ARG, "count must be >= 0");
+    DeviceGuard dg(u->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (count == 0) {   // leave the mode; the host step count takes the device's
+        if (u->device_steps) {
+            int64_t taken = 0;
+            cudaError_t e = cudaMemcpyAsync(&taken, u->step_counter, sizeof(int64_t), cudaMemcpyDeviceToHost, st);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+            if (e != cudaSuccess) return cuda_fail(e, "reading the device step counter");
+            u->t = u->step_base + taken;
+            u->device_steps = false;
+        }
+        return FSDP_OK;
+    }
+    rc = check_hp(hp);
+    if (rc) return rc;
+    if (count > (int64_t(1) << 24)) return fail(FSDP_E_INVALID_ARG, "count must be <= 2^24 steps");
+    if (u->device_steps) {
+        rc = fsdp_adamw_device_steps(u, nullptr, 0, stream);   // fold in the steps taken so far
+        if (rc) return rc;
+    }
+    std::vector<fsdp::AdamWConsts> table(static_cast<size_t>(count));
+    for (int64_t i = 0; i < count; ++i) table[static_cast<size_t>(i)] = adamw_consts(hp, u->t + 1 + i);
+    cudaError_t e = cudaSuccess;
+    if (u->step_counter == nullptr) e = cudaMalloc(reinterpret_cast<void**>(&u->step_counter), 64);
+    if (e == cudaSuccess && u->step_status == nullptr) e = cudaMalloc(reinterpret_cast<void**>(&u->step_status), 64);
+    if (e == cudaSuccess && u->step_table_cap < count) {
+        cudaStreamSynchronize(st);   // the old table may still be in use
+        if (u->step_table) cudaFree(u->step_table);
+        u->step_table = nullptr;
+        u->step_table_cap = 0;
+        e = cudaMalloc(reinterpret_cast<void**>(&u->step_table), sizeof(fsdp::AdamWConsts) * static_cast<size_t>(count));
+        if (e == cudaSuccess) u->step_table_cap = count;
+    }
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(u->step_table, table.data(), sizeof(fsdp::AdamWConsts) * table.size(),
+                            cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);   // `table` is a host temporary
+    if (e == cudaSuccess) e = cudaMemsetAsync(u->step_counter, 0, sizeof(int64_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(u->step_status, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(e == cudaErrorMemoryAllocation ? FSDP_E_OOM : FSDP_E_CUDA,
+                    std::string("device-step set-up: ") + cudaGetErrorString(e));
+    }
+    u->step_count = count;
+    u->step_base = u->t;
+    u->device_steps = true;
+    return FSDP_OK;
+}
+
+int fsdp_adamw_device_status(fsdp_unit* u, int64_t* step, int32_t* exhausted, void* stream) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    if (!u->device_steps) {
+        if (step) *step = u->t;
+        if (exhausted) *exhausted = 0;
+        return FSDP_OK;
+    }
+    DeviceGuard dg(u->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int64_t taken = 0;
+    int32_t status = 0;
+    cudaError_t e = cudaMemcpyAsync(&taken, u->step_counter, sizeof(int64_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&status, u->step_status, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device step counter");
+    if (step) *step = u->step_base + taken;
+    if (exhausted) *exhausted = status;
     return FSDP_OK;
 }
 

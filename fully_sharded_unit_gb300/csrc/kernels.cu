@@ -401,12 +401,36 @@ __device__ __forceinline__ void adamw_elem(float& p, float g, float& m, float& v
     p = __fsub_rn(pd, __fmul_rn(c.step, __fdiv_rn(m, denom)));
 }
 
+// This step's constants.  Device-step mode reads entry *counter of the table
+// (the counter only changes in launch_advance_step, which runs after this
+// kernel on the same stream); a used-up table skips the update and raises
+// the status word instead.
+__device__ __forceinline__ bool step_constants(const StepSource& src, AdamWConsts& c) {
+    if (src.table == nullptr) {
+        c = src.c;
+        return true;
+    }
+    const int64_t i = *src.counter;
+    if (i >= src.count) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) *src.status = 1;
+        return false;
+    }
+    c = src.table[i];
+    return true;
+}
+
+__global__ void advance_step_kernel(int64_t* counter, int64_t count) {
+    if (*counter < count) *counter += 1;
+}
+
 __global__ void __launch_bounds__(kBlock) adamw_kernel(int64_t n8, float* __restrict__ p,
                                                        const float* __restrict__ g,
                                                        float* __restrict__ m,
                                                        float* __restrict__ v,
                                                        uint16_t* __restrict__ shadow,
-                                                       AdamWConsts c) {
+                                                       StepSource src) {
+    AdamWConsts c;
+    if (!step_constants(src, c)) return;   // uniform over the grid
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; i < n8; i += stride) {
         F8 P = ld8_rw(p + 8 * i);
@@ -442,7 +466,9 @@ __global__ void __launch_bounds__(kBlock, sizeof(GT) == 2 ? 3 : 2) reduce_adamw_
                                                               ReduceArgs a, float* __restrict__ gshard,
                                                               float* __restrict__ p, float* __restrict__ m,
                                                               float* __restrict__ v,
-                                                              uint16_t* __restrict__ shadow, AdamWConsts c) {
+                                                              uint16_t* __restrict__ shadow, StepSource src) {
+    AdamWConsts c;
+    if (!step_constants(src, c)) return;   // uniform over the grid
     __shared__ __align__(16) float gsm[kTile];
     const int tid = threadIdx.x;
     const int groups = HYBRID ? a.groups : 1;
@@ -581,7 +607,7 @@ cudaError_t launch_reduce_scatter(const Tile* tiles, int64_t ntiles, const void*
 template <typename GT, int NMAX, bool BF16>
 static cudaError_t launch_ra_t(const Tile* tiles, int64_t ntiles, const void* const* grads,
                                const ReduceArgs& a, float* gshard, float* p, float* m, float* v,
-                               uint16_t* shadow, const AdamWConsts& c, cudaStream_t st) {
+                               uint16_t* shadow, const StepSource& c, cudaStream_t st) {
     GradPtrs<NMAX> gp;
     const int W = a.F * a.groups;
     for (int r = 0; r < NMAX; ++r) gp.p[r] = r < W ? grads[r] : nullptr;
@@ -597,7 +623,7 @@ static cudaError_t launch_ra_t(const Tile* tiles, int64_t ntiles, const void* co
 template <typename GT>
 static cudaError_t launch_ra_dt(const Tile* tiles, int64_t ntiles, const void* const* grads,
                                 const ReduceArgs& a, float* gshard, float* p, float* m, float* v,
-                                uint16_t* shadow, const AdamWConsts& c, cudaStream_t st) {
+                                uint16_t* shadow, const StepSource& c, cudaStream_t st) {
     const bool small = a.F * a.groups <= 64;
     if (a.bf16_reduce)
         return small ? launch_ra_t<GT, 64, true>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st)
@@ -608,7 +634,7 @@ static cudaError_t launch_ra_dt(const Tile* tiles, int64_t ntiles, const void* c
 
 cudaError_t launch_reduce_adamw(const Tile* tiles, int64_t ntiles, const void* const* grads,
                                 int grad_dtype, const ReduceArgs& a, float* gshard, float* p, float* m,
-                                float* v, uint16_t* shadow, const AdamWConsts& c, cudaStream_t st) {
+                                float* v, uint16_t* shadow, const StepSource& c, cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
     if (grad_dtype == FSDP_DTYPE_BF16)
         return launch_ra_dt<uint16_t>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st);
@@ -616,9 +642,14 @@ cudaError_t launch_reduce_adamw(const Tile* tiles, int64_t ntiles, const void* c
 }
 
 cudaError_t launch_adamw(int64_t n8, float* p, const float* g, float* m, float* v,
-                         uint16_t* shadow, const AdamWConsts& c, cudaStream_t st) {
+                         uint16_t* shadow, const StepSource& c, cudaStream_t st) {
     if (n8 == 0) return cudaSuccess;
     adamw_kernel<<<grid_for((n8 + kBlock - 1) / kBlock), kBlock, 0, st>>>(n8, p, g, m, v, shadow, c);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_advance_step(int64_t* counter, int64_t count, cudaStream_t st) {
+    advance_step_kernel<<<1, 1, 0, st>>>(counter, count);
     return cudaGetLastError();
 }
 

@@ -20,6 +20,16 @@ struct AdamWConsts {
     float eps;
 };
 
+// Where AdamW takes one step's constants from: the host-formed `c`, or (for
+// CUDA-graph replay) entry *counter of a device table of consecutive steps.
+struct StepSource {
+    AdamWConsts c;
+    const AdamWConsts* table;   // null: use c
+    const int64_t* counter;     // device: steps taken since the table was made
+    int64_t count;              // table length
+    int32_t* status;            // device: set to 1 when a step finds the table used up
+};
+
 struct ParamSrc {
     const float* ptr;   // parameter's first element
     int64_t offset;     // its FlatParameter offset
@@ -59,10 +69,13 @@ cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t beg
 // unit's segments; a.F * a.groups gradient pointers.
 cudaError_t launch_reduce_adamw(const Tile* tiles, int64_t ntiles, const void* const* grads,
                                 int grad_dtype, const ReduceArgs& a, float* gshard, float* p, float* m,
-                                float* v, uint16_t* shadow, const AdamWConsts& c, cudaStream_t st);
+                                float* v, uint16_t* shadow, const StepSource& c, cudaStream_t st);
 
 // n8: number of 8-element groups in the slab (slab length / 8).
 cudaError_t launch_adamw(int64_t n8, float* p, const float* g, float* m, float* v,
-                         uint16_t* shadow, const AdamWConsts& c, cudaStream_t st);
+                         uint16_t* shadow, const StepSource& c, cudaStream_t st);
+
+// One thread: ++*counter unless the table is used up (device-step mode).
+cudaError_t launch_advance_step(int64_t* counter, int64_t count, cudaStream_t st);
 
 }  // namespace fsdp

@@ -272,7 +272,31 @@ FSDP_API int fsdp_read_global(const fsdp_unit* unit, int which, int64_t begin, i
 FSDP_API int fsdp_read_arena(const fsdp_unit* unit, int which, int rank, void* dst, int64_t* arena_len,
                              void* stream);
 
-/* AdamW step count t (0 after load). */
+/* Device-side AdamW step counter, for replaying a captured CUDA graph.
+ * Normally the step count t lives on the host and each AdamW launch carries
+ * its bias-correction constants, so a captured launch would replay the same
+ * step forever.  This call forms, on the host and with the same formulas as
+ * fsdp_adamw_step, the fp32 constants of the next `count` steps (t+1 ..
+ * t+count, count <= 2^24) into a device table owned by the unit, and switches
+ * the unit to device-step mode: every AdamW launch (fsdp_adamw_step, fsdp_step)
+ * then takes the constants of the step its device counter names, and a one-
+ * thread kernel queued after it advances the counter, so replays step
+ * correctly and give the same results as normal calls.  `hp` is fixed for the
+ * table (the `hp` given to later calls is checked but not used).  A step that
+ * finds the table used up changes nothing and sets the status that
+ * fsdp_adamw_device_status reports.  Allocates (on the first call or when
+ * count grows) and synchronises `stream`: call it before capturing.  count 0
+ * leaves the mode and makes the host step count equal the device's.
+ * fsdp_load_params also leaves the mode. */
+FSDP_API int fsdp_adamw_device_steps(fsdp_unit* unit, const fsdp_adamw_hp* hp, int64_t count, void* stream);
+
+/* In device-step mode: the step count reached on the device and whether a
+ * step found the table used up (synchronises `stream`).  Otherwise the host
+ * step count and 0. */
+FSDP_API int fsdp_adamw_device_status(fsdp_unit* unit, int64_t* step, int32_t* exhausted, void* stream);
+
+/* AdamW step count t (0 after load).  In device-step mode this host copy
+ * counts enqueued steps only; graph replays advance the device counter. */
 FSDP_API int fsdp_get_step_count(const fsdp_unit* unit, int64_t* t);
 FSDP_API int fsdp_set_step_count(fsdp_unit* unit, int64_t t);
 
