@@ -295,17 +295,18 @@ def run_ours(args, world, rank, local):
     K = args.micro_batches
 
     def step():
+        st = torch.cuda.current_stream()   # the capture stream when recording a graph
         for i, u in enumerate(units):
             g = grads if units[i].numel == P_max else [x[:u.numel] for x in grads]
             if K == 1:
-                u.step(g, out, hp, stream)
+                u.step(g, out, hp, st)
                 continue
-            u.allgather(out, stream)
+            u.allgather(out, st)
             if wl.reshard_after_forward:
-                u.allgather(out, stream)
+                u.allgather(out, st)
             for k in range(K):
-                u.reduce_scatter_ex(g, accumulate=k > 0, stream=stream)
-            u.adamw_step(hp, stream)
+                u.reduce_scatter_ex(g, accumulate=k > 0, stream=st)
+            u.adamw_step(hp, st)
 
     for _ in range(args.warmup):
         step()
@@ -358,6 +359,10 @@ def run_ours(args, world, rank, local):
     value_rank = step_bytes * args.steps / (ms * 1e-3) / 1e9
     value = world * step_bytes * args.steps / (ms_max * 1e-3) / 1e9
 
+    graph = None
+    if args.graph and K == 1:
+        graph = run_graph(args, units, step, stream, step_bytes, hp, world, dev)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e and args.micro_batches == 1:
@@ -389,9 +394,41 @@ def run_ours(args, world, rank, local):
                    "gather_source": "fp32 master" if wl.gather_source == "master" else "bf16 shadow",
                    "l2": "inputs larger than L2; no flush", "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "graph": graph,
         "clocks": clk.result,
     }
     print(json.dumps(line), flush=True)
+
+
+def run_graph(args, units, step, stream, step_bytes, hp, world, dev):
+    """The whole step (every unit's fsdp_step) captured once as a CUDA graph
+    and replayed: each unit switches to its device-side AdamW step counter
+    first, so every replay is a correct next step."""
+    from fully_sharded_unit_gb300 import binding as B
+    n = args.warmup + args.steps + 4
+    for u in units:
+        B.fsdp_adamw_device_steps(u.handle, hp, n, stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream(device=dev)):
+        step()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist_max(ev0.elapsed_time(ev1), world, dev)
+    ok = all(not B.fsdp_adamw_device_status(u.handle, stream)[1] for u in units)
+    for u in units:
+        B.fsdp_adamw_device_steps(u.handle, None, 0, stream)
+    del g
+    return {"ms_per_step": ms / args.steps, "value": world * step_bytes * args.steps / (ms * 1e-3) / 1e9,
+            "unit": "GB/s", "steps": args.steps, "table_ok": ok}
 
 
 def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world):
@@ -482,6 +519,9 @@ def main(argv=None):
     ap.add_argument("--micro-batches", type=int, default=1,
                     help="gradient accumulation: reduce-scatters per step (the first overwrites, "
                          "the rest accumulate), then one AdamW")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured once in a CUDA graph and replayed "
+                         "(device-side AdamW step counter)")
     ap.add_argument("--fuse", choices=["on", "off"], default=None,
                     help="override whether fsdp_step fuses reduce-scatter and AdamW")
     args = ap.parse_args(argv)
