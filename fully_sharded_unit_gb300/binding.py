@@ -411,6 +411,8 @@ class Unit:
         self.replicas = info["replicas"]
         self.grad_dtype = grad_dtype
         self.segments = fsdp_unit_segments(self.handle)
+        self._step_key = None
+        self._hp_key = None
         self.shard_len = [0] * self.N
         for s in self.segments:
             self.shard_len[s.rank] += s.len
@@ -445,7 +447,21 @@ class Unit:
         fsdp_adamw_step(self.handle, hp, stream)
 
     def step(self, grads, out, hp, stream=None):
-        fsdp_step(self.handle, grads, out, hp, stream)
+        """fsdp_step.  The pointer array and the hyper-parameter struct are
+        cached by buffer address and values, so repeated steps over the same
+        buffers skip re-validation and re-marshalling."""
+        key = (out.data_ptr(), out.numel(), out.dtype, *[(g.data_ptr(), g.numel(), g.dtype) for g in grads])
+        if key != self._step_key:
+            _check_grads(self.handle, grads)
+            assert out.is_cuda and out.element_size() == 2 and out.is_contiguous() and out.numel() >= self.numel
+            self._step_ptrs = _ptrs(grads)
+            self._step_key = key
+        hkey = tuple(hp.values()) if isinstance(hp, dict) else id(hp)
+        if hkey != self._hp_key:
+            self._hp_struct = _hp(hp)
+            self._hp_key = hkey
+        _check(lib().fsdp_step(self.handle, self._step_ptrs, out.data_ptr(), ctypes.byref(self._hp_struct),
+                               _stream(stream)), "fsdp_step")
 
     def get_state(self, which, rank, device="cuda"):
         dt = torch.int16 if STATES.get(which, which) == FSDP_STATE_SHADOW else torch.float32
