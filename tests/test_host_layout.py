@@ -116,3 +116,20 @@ def test_null_unit_is_rejected():
     assert B.lib().fsdp_allgather(None, None, None) == B.FSDP_E_INVALID_ARG
     assert B.lib().fsdp_step(None, None, None, None, None) == B.FSDP_E_INVALID_ARG
     assert B.lib().fsdp_unit_destroy(None) == B.FSDP_OK
+
+
+def test_new_entry_points_reject_bad_arguments_on_the_host():
+    """Checks that run before any CUDA call, so they hold without a GPU."""
+    import ctypes as C
+    library()
+    L = B.lib()
+    hp = B.AdamWHp(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    assert L.fsdp_adamw_device_steps(None, C.byref(hp), 4, None) == B.FSDP_E_INVALID_ARG
+    assert L.fsdp_adamw_device_status(None, None, None, None) == B.FSDP_E_INVALID_ARG
+    assert L.fsdp_read_arena(None, 0, 0, None, None, None) == B.FSDP_E_INVALID_ARG
+    assert L.fsdp_reduce_scatter_ex(None, None, None, None) == B.FSDP_E_INVALID_ARG
+    assert L.fsdp_zero_grad(None, None) == B.FSDP_E_INVALID_ARG
+    assert L.fsdp_host_device_pointer(None, None) == B.FSDP_E_INVALID_ARG
+    d = C.c_void_p()
+    assert L.fsdp_host_device_pointer(None, C.byref(d)) == B.FSDP_E_INVALID_ARG
+    assert B.fsdp_last_error()          # every failure leaves a reason
