@@ -359,6 +359,15 @@ def run_ours(args, world, rank, local):
     value_rank = step_bytes * args.steps / (ms * 1e-3) / 1e9
     value = world * step_bytes * args.steps / (ms_max * 1e-3) / 1e9
 
+    # the fastest configuration on the same units: bf16-shadow gather and the
+    # fused reduce-scatter + AdamW (identical results, fewer bytes)
+    fastest = None
+    if args.fastest and K == 1 and not (wl.fuse_reduce_adamw and wl.gather_source == "shadow"):
+        fastest = run_variant(args, units, step, stream, hp, world, dev,
+                              wl.with_(gather_source="shadow", fuse_reduce_adamw=True))
+        for u in units:
+            B.fsdp_unit_set_step_options(u.handle, wl.gather_source, wl.fuse_reduce_adamw)
+
     graph = None
     if args.graph and K == 1:
         graph = run_graph(args, units, step, stream, step_bytes, hp, world, dev)
@@ -394,10 +403,33 @@ def run_ours(args, world, rank, local):
                    "gather_source": "fp32 master" if wl.gather_source == "master" else "bf16 shadow",
                    "l2": "inputs larger than L2; no flush", "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "graph": graph,
+        "graph": graph, "fastest_variant": fastest,
         "clocks": clk.result,
     }
     print(json.dumps(line), flush=True)
+
+
+def run_variant(args, units, step, stream, hp, world, dev, vwl):
+    """Time args.steps steps of the same units after switching them to the
+    variant's gather source and fusion; same step, same counted-bytes rules."""
+    from fully_sharded_unit_gb300 import binding as B
+    for u in units:
+        B.fsdp_unit_set_step_options(u.handle, vwl.gather_source, vwl.fuse_reduce_adamw)
+    vbytes = sum(counted_bytes(vwl, i)["step"] for i in range(vwl.n_units))
+    for _ in range(args.warmup):
+        step()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist_max(ev0.elapsed_time(ev1), world, dev)
+    return {"gather_source": vwl.gather_source, "fused_reduce_adamw": vwl.fuse_reduce_adamw,
+            "ms_per_step": ms / args.steps, "counted_bytes_per_step": vbytes,
+            "value": world * vbytes * args.steps / (ms * 1e-3) / 1e9, "unit": "GB/s"}
 
 
 def run_graph(args, units, step, stream, step_bytes, hp, world, dev):
@@ -519,6 +551,9 @@ def main(argv=None):
     ap.add_argument("--micro-batches", type=int, default=1,
                     help="gradient accumulation: reduce-scatters per step (the first overwrites, "
                          "the rest accumulate), then one AdamW")
+    ap.add_argument("--no-fastest", dest="fastest", action="store_false",
+                    help="skip timing the fastest configuration (shadow gather + fused step) "
+                         "on the same units")
     ap.add_argument("--graph", action="store_true",
                     help="also time the step captured once in a CUDA graph and replayed "
                          "(device-side AdamW step counter)")

@@ -106,6 +106,7 @@ _SIGNATURES = {
     "fsdp_set_state": (_I, [_P, _I, _I, _P, _P]),
     "fsdp_read_global": (_I, [_P, _I, _I64, _I64, _P, _P]),
     "fsdp_read_arena": (_I, [_P, _I, _I, _P, _PI64, _P]),
+    "fsdp_unit_set_step_options": (_I, [_P, _I, _I]),
     "fsdp_adamw_device_steps": (_I, [_P, ctypes.POINTER(AdamWHp), _I64, _P]),
     "fsdp_adamw_device_status": (_I, [_P, _PI64, ctypes.POINTER(ctypes.c_int32), _P]),
     "fsdp_get_step_count": (_I, [_P, _PI64]),
@@ -313,6 +314,11 @@ def fsdp_read_arena(h, which, rank, stream=None) -> torch.Tensor:
     if n.value:
         _check(lib().fsdp_read_arena(h, which, rank, dst.data_ptr(), None, _stream(stream)), "fsdp_read_arena")
     return dst
+
+
+def fsdp_unit_set_step_options(h, gather_source="master", fuse_reduce_adamw=False) -> None:
+    _check(lib().fsdp_unit_set_step_options(h, GATHER_SOURCES.get(gather_source, gather_source),
+                                            1 if fuse_reduce_adamw else 0), "fsdp_unit_set_step_options")
 
 
 def fsdp_adamw_device_steps(h, hp, count, stream=None) -> None:

@@ -627,6 +627,16 @@ int fsdp_set_step_count(fsdp_unit* u, int64_t t) {
     return FSDP_OK;
 }
 
+int fsdp_unit_set_step_options(fsdp_unit* u, int gather_source, int fuse_reduce_adamw) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    if (gather_source != FSDP_GATHER_FROM_MASTER && gather_source != FSDP_GATHER_FROM_SHADOW)
+        return fail(FSDP_E_INVALID_ARG, "gather_source must be FSDP_GATHER_FROM_MASTER or _FROM_SHADOW");
+    u->gather_source = gather_source;
+    u->fuse = fuse_reduce_adamw ? 1 : 0;
+    return FSDP_OK;
+}
+
 int fsdp_adamw_device_steps(fsdp_unit* u, const fsdp_adamw_hp* hp, int64_t count, void* stream) {
     int rc = check_unit(u, true);
     if (rc) return rc;

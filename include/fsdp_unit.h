@@ -248,6 +248,13 @@ FSDP_API int fsdp_adamw_step(fsdp_unit* unit, const fsdp_adamw_hp* hp, void* str
 FSDP_API int fsdp_step(fsdp_unit* unit, const void* const* grads_dev, uint16_t* out_bf16_dev,
               const fsdp_adamw_hp* hp, void* stream);
 
+/* Change how fsdp_step runs on an existing unit: gather_source
+ * (FSDP_GATHER_FROM_MASTER or _FROM_SHADOW) and fuse_reduce_adamw, as in
+ * fsdp_unit_config.  Results do not depend on either choice (the shadow always
+ * holds RNE(master), and the fused kernel performs the same operations), only
+ * the bytes moved do.  Takes effect for calls enqueued afterwards. */
+FSDP_API int fsdp_unit_set_step_options(fsdp_unit* unit, int gather_source, int fuse_reduce_adamw);
+
 /* ---- state access (tests, checkpoint / resume) --------------------------- */
 
 /* Copy rank `rank`'s packed shard of state `which` (pads excluded; fp32, or

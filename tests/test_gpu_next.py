@@ -190,3 +190,30 @@ def test_gradients_in_pinned_host_memory():
     with pytest.raises(B.FsdpError) as e:
         B.fsdp_host_device_pointer(torch.zeros(16))          # pageable, not pinned
     assert e.value.code == B.FSDP_E_INVALID_ARG
+
+
+def test_switching_step_options_mid_run_changes_nothing():
+    """fsdp_unit_set_step_options between steps (shadow gather, fused
+    reduce-scatter + AdamW, and back) gives the same bytes as never switching."""
+    wl = workloads.get("ragged_mini_dim0_n7")
+    hp = workloads.hyper(wl)
+    a = B.Unit(wl.shapes(0), "dim0", wl.N)
+    b = B.Unit(wl.shapes(0), "dim0", wl.N)
+    try:
+        params = [p.cuda() for p in workloads.param_tensors(wl, 0)]
+        a.load(params)
+        b.load(params)
+        oa = torch.empty(a.numel, dtype=torch.int16, device="cuda")
+        ob = torch.empty(b.numel, dtype=torch.int16, device="cuda")
+        for s, opts in enumerate([("master", False), ("shadow", True), ("shadow", False), ("master", True)]):
+            B.fsdp_unit_set_step_options(b.handle, *opts)
+            grads = [workloads.grad_tensor(wl, 0, s, r).cuda() for r in range(wl.N)]
+            a.step(grads, oa, hp)
+            b.step(grads, ob, hp)
+            torch.cuda.synchronize()
+            assert torch.equal(oa, ob), s
+        for w in B.STATES:
+            assert torch.equal(a.read_global(w), b.read_global(w)), w
+    finally:
+        a.close()
+        b.close()
