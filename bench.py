@@ -554,8 +554,8 @@ def main(argv=None):
     ap.add_argument("--no-fastest", dest="fastest", action="store_false",
                     help="skip timing the fastest configuration (shadow gather + fused step) "
                          "on the same units")
-    ap.add_argument("--graph", action="store_true",
-                    help="also time the step captured once in a CUDA graph and replayed "
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="skip timing the step captured once in a CUDA graph and replayed "
                          "(device-side AdamW step counter)")
     ap.add_argument("--fuse", choices=["on", "off"], default=None,
                     help="override whether fsdp_step fuses reduce-scatter and AdamW")
