@@ -374,7 +374,7 @@ def run_ours(args, world, rank, local):
 
     # end to end through the public API with host buffers
     e2e = None
-    if not args.no_e2e and args.micro_batches == 1:
+    if not args.no_e2e and args.micro_batches == 1 and not wl.fuse_reduce_adamw:
         e2e = run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world)
 
     cpu = None
@@ -467,45 +467,51 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world)
     """Same metric through the public API with the step's inputs and result in
     pinned host memory.  Every step, for every unit, the N gradients come from
     the host and the gathered bf16 parameters go back to the host:
-      zero_copy -- fsdp_step reads the pinned host gradients directly over the
-                   host link (device addresses from fsdp_host_device_pointer);
+      zero_copy -- the reduce-scatter reads the pinned host gradients directly
+                   over the host link (device addresses from
+                   fsdp_host_device_pointer);
       copy      -- cudaMemcpyAsync of each gradient host->device first.
-    The device->host copy of a unit's gathered parameters runs on a second
-    stream, overlapping the next unit's step; the timed region ends when the
-    last copy has landed."""
+    The unit step is issued as its calls (gather, gather again, reduce-scatter,
+    AdamW: the work of fsdp_step) so that the gathered parameters, final after
+    the first gather, are copied to the host on a second stream while the rest
+    of the unit step runs.  The timed region ends when the last copy has landed."""
     from fully_sharded_unit_gb300 import binding as B
     P_max = grads[0].numel()
     host_grads = [torch.empty(P_max, dtype=grads[0].dtype, pin_memory=True) for _ in grads]
     for h, g in zip(host_grads, grads):
         h.copy_(g)
     host_out = [torch.empty(P_max, dtype=torch.int16, pin_memory=True) for _ in units]
-    outs = [out, torch.empty_like(out)]
+    outs = [(out, torch.empty_like(out)), (torch.empty_like(out), torch.empty_like(out))]
     copy_stream = torch.cuda.Stream(device=dev)
     if args.e2e_mode == "zero_copy":
         unit_grads = [[B.fsdp_host_device_pointer(h[:u.numel]) for h in host_grads] for u in units]
     else:
         unit_grads = [[g[:u.numel] for g in grads] for u in units]
-    free = [None, None]      # events: last D2H copy out of outs[k] finished
+    free = [None, None]      # events: last D2H copy out of outs[k][0] finished
 
     def step():
         done = []
         for i, u in enumerate(units):
-            o = outs[i % 2]
+            first, second = outs[i % 2]
             if free[i % 2] is not None:
                 stream.wait_event(free[i % 2])
             if args.e2e_mode == "copy":
                 for h, g in zip(host_grads, grads):
                     g[:u.numel].copy_(h[:u.numel], non_blocking=True)
-            u.step(unit_grads[i], o, hp, stream)
+            u.allgather(first[:u.numel], stream)
             ready = torch.cuda.Event()
             ready.record(stream)
             copy_stream.wait_event(ready)
             with torch.cuda.stream(copy_stream):
-                host_out[i][:u.numel].copy_(o[:u.numel], non_blocking=True)
+                host_out[i][:u.numel].copy_(first[:u.numel], non_blocking=True)
             ev = torch.cuda.Event()
             ev.record(copy_stream)
             free[i % 2] = ev
             done.append(ev)
+            if wl.reshard_after_forward:
+                u.allgather(second[:u.numel], stream)
+            u.reduce_scatter(unit_grads[i], stream)
+            u.adamw_step(hp, stream)
         for ev in done:
             stream.wait_event(ev)
 
@@ -523,7 +529,7 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world)
     ms = dist_max(ev0.elapsed_time(ev1), world, dev)
     h2d = sum(c["h2d"] for c in cb)
     d2h = sum(c["d2h"] for c in cb)
-    del host_grads, host_out, unit_grads
+    del host_grads, host_out, unit_grads, outs
     return {"value": world * step_bytes * args.e2e_steps / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
             "ms_per_step": ms / args.e2e_steps, "mode": args.e2e_mode}
