@@ -477,7 +477,25 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world)
     of the unit step runs.  The timed region ends when the last copy has landed."""
     from fully_sharded_unit_gb300 import binding as B
     P_max = grads[0].numel()
-    host_grads = [torch.empty(P_max, dtype=grads[0].dtype, pin_memory=True) for _ in grads]
+    # pinned host memory: distinct gradient buffers for every virtual rank when
+    # the host has room for all local ranks' copies; otherwise every virtual
+    # rank reads one shared pinned buffer (the same bytes cross the host link,
+    # only the values repeat)
+    esz = grads[0].element_size()
+    need_distinct = len(grads) * P_max * esz + len(units) * P_max * 2
+    need_shared = P_max * esz + len(units) * P_max * 2
+    local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    avail = host_mem_available()
+    if avail is None or need_distinct * local_ranks <= 0.5 * avail:
+        inputs = "distinct pinned host buffer per virtual rank"
+        host_grads = [torch.empty(P_max, dtype=grads[0].dtype, pin_memory=True) for _ in grads]
+    elif need_shared * local_ranks <= 0.5 * avail:
+        inputs = "one pinned host buffer shared by all virtual ranks (host memory)"
+        shared = torch.empty(P_max, dtype=grads[0].dtype, pin_memory=True)
+        host_grads = [shared] * len(grads)
+    else:
+        return {"value": None, "unit": "GB/s", "skipped": f"host memory: {need_shared * local_ranks / 1e9:.0f} GB "
+                f"of pinned buffers needed, {avail / 1e9:.0f} GB available"}
     for h, g in zip(host_grads, grads):
         h.copy_(g)
     host_out = [torch.empty(P_max, dtype=torch.int16, pin_memory=True) for _ in units]
@@ -532,7 +550,19 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world)
     del host_grads, host_out, unit_grads, outs
     return {"value": world * step_bytes * args.e2e_steps / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "ms_per_step": ms / args.e2e_steps, "mode": args.e2e_mode}
+            "ms_per_step": ms / args.e2e_steps, "mode": args.e2e_mode, "inputs": inputs}
+
+
+def host_mem_available():
+    """MemAvailable in bytes (Linux), or None when unknown."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
 
 
 def main(argv=None):
