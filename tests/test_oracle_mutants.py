@@ -148,3 +148,63 @@ def test_found_flag_misses_nan_caught():
         v, _ = O.reduce_update(G, old, inv_scale)
         return v, bool(np.isinf(v).any())
     _fails(pins.check_reduce_update, upd)
+
+
+def _unit_vs_brute(shard_fn, unshard_fn):
+    """The whole-unit brute-force pin, run against a copy of the oracle whose
+    shard / unshard functions are replaced."""
+    from oracle import brute
+    rng = np.random.default_rng(2)
+    shapes = [(7, 13), (1,), (5,)]
+    params = [rng.uniform(-0.1, 0.1, s).astype(np.float32) for s in shapes]
+    P = 97
+    grads = [[rng.normal(0, 1e-2, P).astype(np.float32) for _ in range(3)]]
+    lay = O.Layout(shapes, 3, "flat")
+    flat = O.flatten(params)
+    sh = shard_fn(flat, lay)
+    gathered = O.bf16_rne(unshard_fn(sh, lay))
+    b = brute.brute_unit_run(shapes, 3, "flat", [p.reshape(-1).tolist() for p in params],
+                             [[g.tolist() for g in grads[0]]], dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                                                                    weight_decay=0.01), raf=False)
+    assert gathered.tolist() == b["gathers"][0][0]
+    for k in range(3):
+        assert sh[k].tolist() == [float(x) for x in np.asarray(flat)[[i for a, c in lay.segments[k] for i in range(a, c)]]]
+
+
+def test_unit_pin_accepts_the_oracle():
+    _unit_vs_brute(O.shard, O.unshard)
+
+
+def test_gather_in_reverse_rank_order_caught():
+    def unshard_rev(shards, lay):
+        out = np.concatenate(list(reversed(shards)))
+        return out
+    _fails(_unit_vs_brute, O.shard, unshard_rev)
+
+
+def test_shard_off_by_one_caught():
+    def shard_shift(flat, lay):
+        out = []
+        for k in range(lay.N):
+            parts = [flat[max(a - 1, 0):max(b - 1, 0)] for a, b in lay.segments[k]]
+            out.append(np.concatenate(parts) if parts else np.zeros(0, flat.dtype))
+        return out
+    with pytest.raises((AssertionError, ValueError)):   # wrong values, or pieces that no longer fit
+        _unit_vs_brute(shard_shift, O.unshard)
+
+
+def test_padded_padding_count_caught():
+    def r(P, N, k):
+        a, b, pad = O.padded_shard_range(P, N, k)
+        return a, b, 0
+    _fails(pins.check_padded_vs_torch_chunk, r, [(15, 16), (5, 4)])
+
+
+def test_hybrid_rank_major_grouping_caught():
+    """Groups must be consecutive ranks (rank i*F + k is rank k of group i);
+    grouping by stride instead changes the rounding."""
+    def r(grads, F):
+        W = len(grads)
+        regrouped = [grads[k * (W // F) + i] for i in range(W // F) for k in range(F)]
+        return O.reduce_full_hybrid(regrouped, F)
+    _fails(pins.check_hybrid_reduce, r, O.reduce_full)
