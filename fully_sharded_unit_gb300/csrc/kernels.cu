@@ -68,6 +68,20 @@ __device__ __forceinline__ uint4 ld8bf_ro(const uint16_t* p) {
     return r;
 }
 
+// 16 bf16 values (read-only input), one 32-byte access
+struct U8 {
+    uint32_t w[8];
+};
+
+__device__ __forceinline__ U8 ld16bf_ro(const uint16_t* p) {
+    U8 r;
+    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]), "=r"(r.w[5]),
+          "=r"(r.w[6]), "=r"(r.w[7])
+        : "l"(p));
+    return r;
+}
+
 __device__ __forceinline__ void st8bf(uint16_t* p, uint4 r) {
     asm volatile("st.global.L1::no_allocate.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(r.x),
                  "r"(r.y), "r"(r.z), "r"(r.w));
@@ -103,12 +117,14 @@ struct TileSplit {
     int tail;   // elements after the last group
 };
 
+// A-element groups (A = 8, or 16 for the bf16-gradient reduce-scatter).
+template <int A = 8>
 __device__ __forceinline__ TileSplit split_tile(int64_t g, int len) {
     TileSplit t;
-    t.head = static_cast<int>((8 - (g & 7)) & 7);
+    t.head = static_cast<int>((A - (g & (A - 1))) & (A - 1));
     if (t.head > len) t.head = len;
-    t.nvec = (len - t.head) >> 3;
-    t.tail = len - t.head - 8 * t.nvec;
+    t.nvec = (len - t.head) / A;
+    t.tail = len - t.head - A * t.nvec;
     return t;
 }
 
@@ -337,6 +353,93 @@ __device__ __forceinline__ F8 reduce8(const GradPtrs<NMAX>& gp, const ReduceArgs
     return tot;
 }
 
+// Ranks folded per batch in the 16-wide path: 4 x 32 bytes in flight per
+// thread, as many bytes as the 8-wide path's 8 x 16, in half the registers.
+constexpr int kBatch16 = 4;
+
+// Sixteen consecutive bf16-gradient elements (one 32-byte load per rank), same
+// order of operations as reduce8.  bf16 inputs are exact, so the bf16
+// reduction rounds only the partial sums and the quotient.
+template <int NMAX, bool BF16>
+__device__ __forceinline__ void reduce16(const GradPtrs<NMAX>& gp, const ReduceArgs& a, int groups,
+                                         float fW, int64_t gi, F8& out0, F8& out1) {
+    F8 t0, t1;
+    for (int grp = 0; grp < groups; ++grp) {
+        const int base = grp * a.F;
+        F8 a0, a1;
+        for (int r0 = 0; r0 < a.F; r0 += kBatch16) {
+            U8 x[kBatch16];
+#pragma unroll
+            for (int b = 0; b < kBatch16; ++b)
+                if (r0 + b < a.F) x[b] = ld16bf_ro(static_cast<const uint16_t*>(gp.p[base + r0 + b]) + gi);
+#pragma unroll
+            for (int b = 0; b < kBatch16; ++b) {
+                if (r0 + b < a.F) {
+                    F8 w0, w1;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        widen2(x[b].w[q], w0.v[2 * q], w0.v[2 * q + 1]);
+                        widen2(x[b].w[4 + q], w1.v[2 * q], w1.v[2 * q + 1]);
+                    }
+                    if (r0 + b == 0) {
+                        a0 = w0;
+                        a1 = w1;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            a0.v[e] = __fadd_rn(a0.v[e], w0.v[e]);
+                            a1.v[e] = __fadd_rn(a1.v[e], w1.v[e]);
+                            if (BF16) {
+                                a0.v[e] = round_bf16(a0.v[e]);
+                                a1.v[e] = round_bf16(a1.v[e]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        if (grp == 0) {
+            t0 = a0;
+            t1 = a1;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                t0.v[e] = __fadd_rn(t0.v[e], a0.v[e]);
+                t1.v[e] = __fadd_rn(t1.v[e], a1.v[e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        t0.v[e] = __fdiv_rn(t0.v[e], fW);
+        t1.v[e] = __fdiv_rn(t1.v[e], fW);
+        if (BF16) {
+            t0.v[e] = round_bf16(t0.v[e]);
+            t1.v[e] = round_bf16(t1.v[e]);
+        }
+    }
+    out0 = t0;
+    out1 = t1;
+}
+
+// Optional unscale / accumulation / non-finite check of eight results.
+__device__ __forceinline__ void post8(F8& x, const float* dst, bool post, const ReduceArgs& a,
+                                      bool check, bool& bad) {
+    if (post) {
+        F8 old;
+        if (a.accumulate) old = ld8_rw(dst);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if (a.scale) x.v[e] = __fmul_rn(x.v[e], a.inv_scale);
+            if (a.accumulate) x.v[e] = __fadd_rn(old.v[e], x.v[e]);
+        }
+    }
+    if (check) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) bad |= not_finite(x.v[e]);
+    }
+}
+
 // EXT = false compiles the plain reduce-scatter (one group, no unscale, no
 // accumulation, no flag) with the fewest registers; EXT = true adds hybrid
 // groups and the post-reduction options.
@@ -349,14 +452,17 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_kernel(const Tile* __re
     const float fW = static_cast<float>(a.F * groups);
     const bool post = EXT && (a.scale || a.accumulate);
     int32_t* const found = EXT ? a.found : nullptr;
+    // bf16 gradients: 16-element groups, one 32-byte load per rank (measured
+    // 7.46 TB/s against 7.24 TB/s with 16-byte loads on the minGPT unit)
+    constexpr int A = std::is_same<GT, uint16_t>::value ? 16 : 8;
     bool bad = false;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const Tile tl = tiles[t];
-        const TileSplit sp = split_tile(tl.g, tl.len);
+        const TileSplit sp = split_tile<A>(tl.g, tl.len);
         // scalar head and tail
         int j = -1;
         if (tid < sp.head) j = tid;
-        else if (tid >= 8 && tid < 8 + sp.tail) j = sp.head + 8 * sp.nvec + (tid - 8);
+        else if (tid >= A && tid < A + sp.tail) j = sp.head + A * sp.nvec + (tid - A);
         if (j >= 0) {
             float x = reduce1<GT, NMAX, BF16>(gp, a, groups, fW, tl.g + j);
             if (post && a.scale) x = __fmul_rn(x, a.inv_scale);
@@ -364,25 +470,23 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_kernel(const Tile* __re
             if (found != nullptr) bad |= not_finite(x);
             gshard[tl.s + j] = x;
         }
-        // 8-element groups
+        // A-element groups
         const int64_t g0 = tl.g + sp.head;
         float* dst = gshard + tl.s + sp.head;
         for (int v = tid; v < sp.nvec; v += kBlock) {
-            F8 x = reduce8<GT, NMAX, BF16>(gp, a, groups, fW, g0 + 8 * static_cast<int64_t>(v));
-            if (post) {
-                F8 old;
-                if (a.accumulate) old = ld8_rw(dst + 8 * v);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    if (a.scale) x.v[e] = __fmul_rn(x.v[e], a.inv_scale);
-                    if (a.accumulate) x.v[e] = __fadd_rn(old.v[e], x.v[e]);
-                }
+            float* d = dst + A * v;
+            if constexpr (A == 16) {
+                F8 x0, x1;
+                reduce16<NMAX, BF16>(gp, a, groups, fW, g0 + 16 * static_cast<int64_t>(v), x0, x1);
+                post8(x0, d, post, a, found != nullptr, bad);
+                post8(x1, d + 8, post, a, found != nullptr, bad);
+                st8(d, x0);
+                st8(d + 8, x1);
+            } else {
+                F8 x = reduce8<GT, NMAX, BF16>(gp, a, groups, fW, g0 + 8 * static_cast<int64_t>(v));
+                post8(x, d, post, a, found != nullptr, bad);
+                st8(d, x);
             }
-            if (found != nullptr) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) bad |= not_finite(x.v[e]);
-            }
-            st8(dst + 8 * v, x);
         }
     }
     if (found != nullptr) {   // uniform across the CTA
