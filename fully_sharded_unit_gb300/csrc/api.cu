@@ -119,9 +119,20 @@ void free_unit(fsdp_unit* u) {
 template <typename F>
 int profiled_launch(fsdp_unit* u, int kind, cudaStream_t st, const char* what, F&& fn) {
     ProfRecord rec{kind, nullptr, nullptr};
-    if (u->profiling) {
-        if (cudaEventCreate(&rec.start) != cudaSuccess || cudaEventCreate(&rec.stop) != cudaSuccess)
+    bool timed = u->profiling;
+    if (timed) {   // launches recorded into a CUDA graph are not timed
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+            cudaGetLastError();
+            timed = false;
+        }
+    }
+    if (timed) {
+        if (cudaEventCreate(&rec.start) != cudaSuccess) return fail(FSDP_E_CUDA, "cudaEventCreate failed");
+        if (cudaEventCreate(&rec.stop) != cudaSuccess) {
+            cudaEventDestroy(rec.start);
             return fail(FSDP_E_CUDA, "cudaEventCreate failed");
+        }
         cudaEventRecord(rec.start, st);
     }
     cudaError_t e = fn();
@@ -130,7 +141,7 @@ int profiled_launch(fsdp_unit* u, int kind, cudaStream_t st, const char* what, F
         if (rec.stop) cudaEventDestroy(rec.stop);
         return cuda_fail(e, what);
     }
-    if (u->profiling) {
+    if (timed) {
         cudaEventRecord(rec.stop, st);
         u->prof.push_back(rec);
     }
@@ -357,8 +368,10 @@ int fsdp_unit_create(int nparams, const int* ndims, const int64_t* dims,
         return fail(FSDP_E_INVALID_ARG, "reduce_dtype must be FSDP_DTYPE_F32 or FSDP_DTYPE_BF16");
     if (cfg->gather_source != FSDP_GATHER_FROM_MASTER && cfg->gather_source != FSDP_GATHER_FROM_SHADOW)
         return fail(FSDP_E_INVALID_ARG, "gather_source must be FSDP_GATHER_FROM_MASTER or _FROM_SHADOW");
+    if (cfg->num_ranks < 1 || cfg->num_ranks > fsdp::kMaxRanks)
+        return fail(FSDP_E_INVALID_ARG, "num_ranks must be in [1, 1024]");
     const int replicas = cfg->replicas == 0 ? 1 : cfg->replicas;
-    if (replicas < 1 || cfg->num_ranks < 1 || replicas > fsdp::kMaxRanks / cfg->num_ranks)
+    if (replicas < 1 || replicas > fsdp::kMaxRanks / cfg->num_ranks)
         return fail(FSDP_E_INVALID_ARG, "replicas must be >= 1 with num_ranks * replicas <= 1024");
     if (replicas > 1 && cfg->reduce_dtype == FSDP_DTYPE_BF16)
         return fail(FSDP_E_INVALID_ARG, "bf16 reduction is supported with replicas == 1 only");
@@ -478,6 +491,7 @@ int fsdp_allgather(fsdp_unit* u, uint16_t* out, void* stream) {
     if (rc == FSDP_OK) rc = check_out(out);
     if (rc) return rc;
     DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     return enqueue_gather(u, out, static_cast<cudaStream_t>(stream));
 }
 
@@ -486,6 +500,7 @@ int fsdp_reduce_scatter(fsdp_unit* u, const void* const* grads, void* stream) {
     if (rc == FSDP_OK) rc = check_grads(u, grads);
     if (rc) return rc;
     DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     return enqueue_reduce_scatter(u, grads, nullptr, static_cast<cudaStream_t>(stream));
 }
 
@@ -496,6 +511,7 @@ int fsdp_reduce_scatter_ex(fsdp_unit* u, const void* const* grads, const fsdp_rs
     if (rc == FSDP_OK) rc = check_rs_options(opt);
     if (rc) return rc;
     DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     return enqueue_reduce_scatter(u, grads, opt, static_cast<cudaStream_t>(stream));
 }
 
@@ -503,6 +519,7 @@ int fsdp_zero_grad(fsdp_unit* u, void* stream) {
     int rc = check_unit(u, true);
     if (rc) return rc;
     DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     cudaError_t e = cudaMemsetAsync(u->grad, 0, static_cast<size_t>(u->plan.slab_len) * 4,
                                     static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "zeroing the gradient shards");
@@ -513,6 +530,7 @@ int fsdp_adamw_step(fsdp_unit* u, const fsdp_adamw_hp* hp, void* stream) {
     if (rc == FSDP_OK) rc = check_hp(hp);
     if (rc) return rc;
     DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     return enqueue_adamw(u, hp, static_cast<cudaStream_t>(stream));
 }
 
@@ -524,6 +542,7 @@ int fsdp_step(fsdp_unit* u, const void* const* grads, uint16_t* out, const fsdp_
     if (rc == FSDP_OK) rc = check_hp(hp);
     if (rc) return rc;
     DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     rc = enqueue_gather(u, out, st);                       // forward
     if (rc == FSDP_OK && u->raf) rc = enqueue_gather(u, out, st);   // backward re-gather
@@ -542,6 +561,7 @@ static int copy_state(const fsdp_unit* u, int which, int rank, void* ext, bool t
     if (base == nullptr) return fail(FSDP_E_INVALID_ARG, "unknown state");
     if (ext == nullptr && u->plan.shard_len[rank] > 0) return fail(FSDP_E_INVALID_ARG, "buffer is null");
     DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t abase = u->plan.arena_base[rank];
     for (int64_t i = u->plan.rank_first_seg[rank]; i < u->plan.rank_first_seg[rank + 1]; ++i) {
@@ -578,6 +598,7 @@ int fsdp_read_global(const fsdp_unit* u, int which, int64_t begin, int64_t count
     if (base == nullptr) return fail(FSDP_E_INVALID_ARG, "unknown state");
     if (count > 0 && dst == nullptr) return fail(FSDP_E_INVALID_ARG, "dst is null");
     DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t end = begin + count;
     for (const fsdp_segment& s : u->plan.segs) {
@@ -604,6 +625,7 @@ int fsdp_read_arena(const fsdp_unit* u, int which, int rank, void* dst, int64_t*
     if (arena_len) *arena_len = n;
     if (dst == nullptr) return FSDP_OK;   // size query
     DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     cudaError_t e = cudaMemcpyAsync(dst, base + static_cast<size_t>(u->plan.arena_base[rank]) * esz,
                                     static_cast<size_t>(n) * esz, cudaMemcpyDefault,
                                     static_cast<cudaStream_t>(stream));
@@ -642,6 +664,7 @@ int fsdp_adamw_device_steps(fsdp_unit* u, const fsdp_adamw_hp* hp, int64_t count
     if (rc) return rc;
     if (count < 0) return fail(FSDP_E_INVALID_ARG, "count must be >= 0");
     DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (count == 0) {   // leave the mode; the host step count takes the device's
         if (u->device_steps) {
@@ -700,6 +723,7 @@ int fsdp_adamw_device_status(fsdp_unit* u, int64_t* step, int32_t* exhausted, vo
         return FSDP_OK;
     }
     DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int64_t taken = 0;
     int32_t status = 0;
@@ -768,6 +792,7 @@ int fsdp_profile_read(fsdp_unit* u, int kernel, double* total_ms, int64_t* launc
     if (rc) return rc;
     if (kernel < 0 || kernel >= FSDP_KERNEL_COUNT) return fail(FSDP_E_INVALID_ARG, "unknown kernel");
     DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     double sum = 0.0;
     int64_t n = 0;
     for (const ProfRecord& r : u->prof) {
@@ -788,6 +813,7 @@ int fsdp_profile_reset(fsdp_unit* u) {
     int rc = check_unit(u, false);
     if (rc) return rc;
     DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     for (auto& r : u->prof) {
         cudaEventSynchronize(r.stop);
         cudaEventDestroy(r.start);

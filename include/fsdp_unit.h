@@ -328,7 +328,8 @@ FSDP_API int fsdp_memory_report(const fsdp_unit* unit, int rank, int64_t* param_
 /* ---- profiling ------------------------------------------------------------- */
 
 /* While enabled, every kernel the unit launches is bracketed by CUDA events
- * recorded on its launch stream.  fsdp_profile_read waits for the recorded
+ * recorded on its launch stream (launches on a stream that is being captured
+ * into a CUDA graph are not timed).  fsdp_profile_read waits for the recorded
  * events and returns, for one FSDP_KERNEL_* kind, the summed device time in
  * milliseconds and the launch count since the last reset.  Disabling keeps
  * the records; fsdp_profile_reset drops them. */
