@@ -1,13 +1,17 @@
-// Per-unit FSDP kernels for sm_103a: shard-in, gather+cast, reduce-scatter,
-// AdamW.  All four are HBM-bandwidth bound streaming passes; none is a
-// contraction, so no tensor cores are involved.
+// Per-unit FSDP kernels for sm_103a: shard-in, gather+cast (from the fp32
+// master or the bf16 shadow), reduce-scatter, AdamW, the fused reduce-scatter
+// + AdamW, a range cast and the device step counter.  All are HBM-bandwidth
+// bound streaming passes; none is a contraction, so no tensor cores are
+// involved.
 //
 // Memory access: an 8-element group is one 256-bit fp32 access
-// (ld/st .v8.f32) or one 128-bit bf16 access (.v4.b32).  Segment-driven
-// kernels walk a tile table (see plan.hpp): a tile never spans two segments,
-// and because arena slots are congruent to global indices modulo 32 elements,
-// a group that is aligned in the unsharded buffer is aligned in the arena.
-// Each tile has at most 7 unaligned head and 7 tail elements, done scalar.
+// (ld/st .v8.f32) or one 128-bit bf16 access (.v4.b32); the bf16-gradient
+// reduce-scatter reads 16-element groups, one 256-bit access per rank.
+// Segment-driven kernels walk a tile table (see plan.hpp): a tile never spans
+// two segments, and because arena slots are congruent to global indices
+// modulo 32 elements, a group that is aligned in the unsharded buffer is
+// aligned in the arena.  Each tile has at most A-1 unaligned head and A-1
+// tail elements (A = 8 or 16), done scalar.
 //
 // Numerics: every floating-point operation is an explicitly rounded
 // intrinsic (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so nothing is
