@@ -26,6 +26,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import shutil
 import statistics
 import subprocess
@@ -72,8 +73,14 @@ def measured_peak():
 
 
 def kernel_source_sha() -> str:
-    with open(os.path.join(ROOT, "fully_sharded_unit_gb300", "csrc", "kernels.cu"), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256[:16] of csrc/kernels.cu with comments and whitespace removed, so
+    that an edit of the comments alone keeps a capture valid."""
+    with open(os.path.join(ROOT, "fully_sharded_unit_gb300", "csrc", "kernels.cu")) as f:
+        code = f.read()
+    code = re.sub(r"/\*.*?\*/", "", code, flags=re.S)
+    code = re.sub(r"//[^\n]*", "", code)
+    code = re.sub(r"\s+", " ", code).strip()
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str):
