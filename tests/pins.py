@@ -20,6 +20,7 @@ What pins what:
 from __future__ import annotations
 
 import math
+from fractions import Fraction
 
 import numpy as np
 import torch
@@ -328,6 +329,76 @@ def check_bf16_reduce_vs_torch(reduce_full_bf16, seed=0):
     for N in (2, 5, 8):
         grads = [np.full(10, r + 1, np.float32) for r in range(N)]
         assert np.all(reduce_full_bf16(grads) == np.float32((N + 1) / 2))
+
+
+def _round_bf16_exact(x: Fraction, sign: float) -> float:
+    """The bf16 value nearest to the exact rational x (ties to an even last
+    significand bit; an unbounded-exponent result of 2**128 or more is
+    infinity).  `sign` gives the sign of a zero result."""
+    if x == 0:
+        return math.copysign(0.0, sign)
+    s = -1.0 if x < 0 else 1.0
+    ax = abs(x)
+    e = ax.numerator.bit_length() - ax.denominator.bit_length()
+    while Fraction(2) ** e > ax:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= ax:
+        e += 1
+    ulp = Fraction(2) ** (max(e, -126) - 7)      # 8 significand bits; subnormals below 2**-126
+    q = ax / ulp
+    n = q.numerator // q.denominator
+    rem = q - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    val = n * ulp
+    if val >= Fraction(2) ** 128:
+        return s * math.inf
+    return math.copysign(float(val), s)
+
+
+def check_bf16_reduce_exact(reduce_full_bf16, seed=0):
+    """bf16 arithmetic from its definition: each partial sum of the rank-order
+    fold and the final division by N is the exact rational result rounded
+    once to bf16.  Inputs are bf16 bit patterns of every exponent (subnormals,
+    zeros of both signs, the largest finite values) plus pairs whose exponents
+    differ by 0..20, so that sums land near bf16 rounding midpoints; a
+    missing, doubled or misplaced rounding fails here."""
+    rng = np.random.default_rng(seed)
+
+    def finite_patterns(n):
+        b = rng.integers(0, 1 << 16, n, dtype=np.uint32).astype(np.uint16)
+        inf_nan = (b & 0x7F80) == 0x7F80
+        b[inf_nan] &= 0xBFFF                     # exponent 0xFF -> 0x7F: finite
+        return b
+
+    def value(h):
+        return float(np.uint32(int(h) << 16).view(np.float32))
+
+    cases = []
+    for N in (2, 3, 8):
+        cases.append([finite_patterns(4000) for _ in range(N)])
+    a = finite_patterns(4000) & 0x807F | (rng.integers(40, 200, 4000).astype(np.uint16) << 7)
+    d = rng.integers(0, 21, 4000).astype(np.uint16)
+    b = finite_patterns(4000) & 0x807F | (((a >> 7) & 0xFF) - d) << 7
+    cases.append([a, b])
+    cases.append([np.array([0x8000, 0x8000, 0x0000, 0x7F7F, 0xFF7F, 0x0001], np.uint16),
+                  np.array([0x8000, 0x0000, 0x8000, 0x7F7F, 0x7F7F, 0x8001], np.uint16)])
+    for grads in cases:
+        N = len(grads)
+        with np.errstate(over="ignore"):
+            got = reduce_full_bf16(grads)
+        for i in range(grads[0].size):
+            acc = value(grads[0][i])
+            for r in range(1, N):
+                x = value(grads[r][i])
+                if math.isinf(acc):
+                    continue                     # finite inputs: inf + x stays inf
+                zero_sign = -1.0 if (math.copysign(1.0, acc) < 0 and math.copysign(1.0, x) < 0) else 1.0
+                acc = _round_bf16_exact(Fraction(acc) + Fraction(x), zero_sign)
+            want = acc if math.isinf(acc) else _round_bf16_exact(Fraction(acc) / N, math.copysign(1.0, acc))
+            w = np.float32(want).view(np.uint32)
+            g = got[i].view(np.uint32)
+            assert w == g, (N, i, [hex(int(gr[i])) for gr in grads], float(got[i]), want)
 
 
 def check_reduce_update(reduce_update):

@@ -135,6 +135,27 @@ def test_bf16_reduce_in_fp32_caught():
     def r(grads):
         return O.bf16_to_f32(O.bf16_rne(O.reduce_full(grads)))
     _fails(pins.check_bf16_reduce_vs_torch, r)
+    _fails(pins.check_bf16_reduce_exact, r)
+
+
+def test_bf16_reduce_unrounded_quotient_caught():
+    def r(grads):
+        acc = O.bf16_to_f32(O.bf16_rne(O.upcast_grad(grads[0])))
+        for g in grads[1:]:
+            acc = O.bf16_to_f32(O.bf16_rne((acc + O.bf16_to_f32(O.bf16_rne(O.upcast_grad(g)))).astype(np.float32)))
+        return (acc / np.float32(len(grads))).astype(np.float32)
+    _fails(pins.check_bf16_reduce_exact, r)
+
+
+def test_bf16_reduce_truncating_partial_sums_caught():
+    def trunc(x):
+        return (np.asarray(x, np.float32).view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)
+    def r(grads):
+        acc = O.bf16_to_f32(O.bf16_rne(O.upcast_grad(grads[0])))
+        for g in grads[1:]:
+            acc = trunc((acc + O.bf16_to_f32(O.bf16_rne(O.upcast_grad(g)))).astype(np.float32))
+        return O.bf16_to_f32(O.bf16_rne((acc / np.float32(len(grads))).astype(np.float32)))
+    _fails(pins.check_bf16_reduce_exact, r)
 
 
 def test_accumulate_overwrites_caught():

@@ -37,6 +37,10 @@ def test_bf16_reduction_vs_torch():
     pins.check_bf16_reduce_vs_torch(O.reduce_full_bf16)
 
 
+def test_bf16_reduction_vs_exact_rounding():
+    pins.check_bf16_reduce_exact(O.reduce_full_bf16)
+
+
 def test_reduce_update():
     pins.check_reduce_update(O.reduce_update)
 
