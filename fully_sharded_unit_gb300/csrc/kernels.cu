@@ -114,6 +114,21 @@ __device__ __forceinline__ void widen2(uint32_t w, float& lo, float& hi) {
     hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
+// Correctly rounded (RNE) addition of two bf16 pairs.  It equals the fp32 sum
+// rounded once to bf16: the exact sum of two bf16 values rounded to fp32 and
+// then to bf16 cannot differ from it rounded straight to bf16, because fp32
+// carries at least 2*8+2 significant bits (double rounding is innocuous).
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// bf16 partial sums of 8 elements, 4 packed pairs, folded in one rank order.
+struct B8 {
+    uint32_t w[4];
+};
+
 // Split of a tile into an unaligned head, 8-element groups and a tail.
 struct TileSplit {
     int head;   // elements before the first 8-aligned global index
@@ -250,6 +265,11 @@ struct GradIO<float> {
         return Group{ld8_ro(static_cast<const float*>(base) + i)};
     }
     static __device__ __forceinline__ void widen(const Group& g, F8& out) { out = g.f; }
+    // the group rounded to bf16 pairs (RNE), for the bf16 reduction
+    static __device__ __forceinline__ B8 pack(const Group& g) {
+        return B8{{pack_bf16x2(g.f.v[0], g.f.v[1]), pack_bf16x2(g.f.v[2], g.f.v[3]),
+                   pack_bf16x2(g.f.v[4], g.f.v[5]), pack_bf16x2(g.f.v[6], g.f.v[7])}};
+    }
 };
 
 template <>
@@ -269,6 +289,7 @@ struct GradIO<uint16_t> {
         widen2(g.w.z, out.v[4], out.v[5]);
         widen2(g.w.w, out.v[6], out.v[7]);
     }
+    static __device__ __forceinline__ B8 pack(const Group& g) { return B8{{g.w.x, g.w.y, g.w.z, g.w.w}}; }
 };
 
 // fp32 value rounded to bf16 (RNE) and widened back: one bf16 rounding.
@@ -307,54 +328,87 @@ __device__ __forceinline__ float reduce1(const GradPtrs<NMAX>& gp, const ReduceA
     return __fdiv_rn(tot, fW);
 }
 
+// bf16 reduction of one aligned group (reduce_dtype bf16, one group: the host
+// rejects it with replicas): inputs rounded to bf16 (exact for bf16
+// gradients), the rank-order partial sums kept as packed bf16 pairs, then
+// the quotient by F rounded to bf16.  Same values as rounding every fp32
+// partial sum (see add_bf16x2).
+template <int W>
+struct BGroup {
+    uint32_t w[W];
+};
+
+template <int W>
+__device__ __forceinline__ void finish_bf16(const BGroup<W>& acc, float fW, F8* out) {
+#pragma unroll
+    for (int q = 0; q < W; ++q) {
+        F8& o = out[q / 4];
+        widen2(acc.w[q], o.v[2 * (q % 4)], o.v[2 * (q % 4) + 1]);
+    }
+#pragma unroll
+    for (int h = 0; h < W / 4; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) out[h].v[e] = round_bf16(__fdiv_rn(out[h].v[e], fW));
+}
+
 // Eight consecutive elements (an aligned group), same order of operations.
 template <typename GT, int NMAX, bool BF16>
 __device__ __forceinline__ F8 reduce8(const GradPtrs<NMAX>& gp, const ReduceArgs& a, int groups,
                                       float fW, int64_t gi) {
     using IO = GradIO<GT>;
     F8 tot;
-    for (int grp = 0; grp < groups; ++grp) {
-        const int base = grp * a.F;
-        F8 acc;
+    if constexpr (BF16) {
+        BGroup<4> acc;
         for (int r0 = 0; r0 < a.F; r0 += kBatch) {
             typename IO::Group x[kBatch];
 #pragma unroll
             for (int b = 0; b < kBatch; ++b)
-                if (r0 + b < a.F) x[b] = IO::load8(gp.p[base + r0 + b], gi);
+                if (r0 + b < a.F) x[b] = IO::load8(gp.p[r0 + b], gi);
 #pragma unroll
             for (int b = 0; b < kBatch; ++b) {
                 if (r0 + b < a.F) {
-                    F8 w;
-                    IO::widen(x[b], w);
-                    if (BF16 && !std::is_same<GT, uint16_t>::value) {   // bf16 inputs are exact
+                    const B8 w = IO::pack(x[b]);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) w.v[e] = round_bf16(w.v[e]);
-                    }
-                    if (r0 + b == 0) {
-                        acc = w;
-                    } else {
+                    for (int q = 0; q < 4; ++q) acc.w[q] = r0 + b == 0 ? w.w[q] : add_bf16x2(acc.w[q], w.w[q]);
+                }
+            }
+        }
+        finish_bf16<4>(acc, fW, &tot);
+        return tot;
+    } else {
+        for (int grp = 0; grp < groups; ++grp) {
+            const int base = grp * a.F;
+            F8 acc;
+            for (int r0 = 0; r0 < a.F; r0 += kBatch) {
+                typename IO::Group x[kBatch];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            acc.v[e] = __fadd_rn(acc.v[e], w.v[e]);
-                            if (BF16) acc.v[e] = round_bf16(acc.v[e]);
+                for (int b = 0; b < kBatch; ++b)
+                    if (r0 + b < a.F) x[b] = IO::load8(gp.p[base + r0 + b], gi);
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    if (r0 + b < a.F) {
+                        F8 w;
+                        IO::widen(x[b], w);
+                        if (r0 + b == 0) {
+                            acc = w;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc.v[e] = __fadd_rn(acc.v[e], w.v[e]);
                         }
                     }
                 }
             }
-        }
-        if (grp == 0) {
-            tot = acc;
-        } else {
+            if (grp == 0) {
+                tot = acc;
+            } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) tot.v[e] = __fadd_rn(tot.v[e], acc.v[e]);
+                for (int e = 0; e < 8; ++e) tot.v[e] = __fadd_rn(tot.v[e], acc.v[e]);
+            }
         }
-    }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        tot.v[e] = __fdiv_rn(tot.v[e], fW);
-        if (BF16) tot.v[e] = round_bf16(tot.v[e]);
+        for (int e = 0; e < 8; ++e) tot.v[e] = __fdiv_rn(tot.v[e], fW);
+        return tot;
     }
-    return tot;
 }
 
 // Ranks folded per batch in the 16-wide path: 4 x 32 bytes in flight per
@@ -362,68 +416,82 @@ __device__ __forceinline__ F8 reduce8(const GradPtrs<NMAX>& gp, const ReduceArgs
 constexpr int kBatch16 = 4;
 
 // Sixteen consecutive bf16-gradient elements (one 32-byte load per rank), same
-// order of operations as reduce8.  bf16 inputs are exact, so the bf16
-// reduction rounds only the partial sums and the quotient.
+// order of operations as reduce8.
 template <int NMAX, bool BF16>
 __device__ __forceinline__ void reduce16(const GradPtrs<NMAX>& gp, const ReduceArgs& a, int groups,
                                          float fW, int64_t gi, F8& out0, F8& out1) {
-    F8 t0, t1;
-    for (int grp = 0; grp < groups; ++grp) {
-        const int base = grp * a.F;
-        F8 a0, a1;
+    if constexpr (BF16) {
+        BGroup<8> acc;
         for (int r0 = 0; r0 < a.F; r0 += kBatch16) {
             U8 x[kBatch16];
 #pragma unroll
             for (int b = 0; b < kBatch16; ++b)
-                if (r0 + b < a.F) x[b] = ld16bf_ro(static_cast<const uint16_t*>(gp.p[base + r0 + b]) + gi);
+                if (r0 + b < a.F) x[b] = ld16bf_ro(static_cast<const uint16_t*>(gp.p[r0 + b]) + gi);
 #pragma unroll
             for (int b = 0; b < kBatch16; ++b) {
                 if (r0 + b < a.F) {
-                    F8 w0, w1;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        widen2(x[b].w[q], w0.v[2 * q], w0.v[2 * q + 1]);
-                        widen2(x[b].w[4 + q], w1.v[2 * q], w1.v[2 * q + 1]);
-                    }
-                    if (r0 + b == 0) {
-                        a0 = w0;
-                        a1 = w1;
-                    } else {
+                    for (int q = 0; q < 8; ++q)
+                        acc.w[q] = r0 + b == 0 ? x[b].w[q] : add_bf16x2(acc.w[q], x[b].w[q]);
+                }
+            }
+        }
+        F8 o[2];
+        finish_bf16<8>(acc, fW, o);
+        out0 = o[0];
+        out1 = o[1];
+        return;
+    } else {
+        F8 t0, t1;
+        for (int grp = 0; grp < groups; ++grp) {
+            const int base = grp * a.F;
+            F8 a0, a1;
+            for (int r0 = 0; r0 < a.F; r0 += kBatch16) {
+                U8 x[kBatch16];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            a0.v[e] = __fadd_rn(a0.v[e], w0.v[e]);
-                            a1.v[e] = __fadd_rn(a1.v[e], w1.v[e]);
-                            if (BF16) {
-                                a0.v[e] = round_bf16(a0.v[e]);
-                                a1.v[e] = round_bf16(a1.v[e]);
+                for (int b = 0; b < kBatch16; ++b)
+                    if (r0 + b < a.F) x[b] = ld16bf_ro(static_cast<const uint16_t*>(gp.p[base + r0 + b]) + gi);
+#pragma unroll
+                for (int b = 0; b < kBatch16; ++b) {
+                    if (r0 + b < a.F) {
+                        F8 w0, w1;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            widen2(x[b].w[q], w0.v[2 * q], w0.v[2 * q + 1]);
+                            widen2(x[b].w[4 + q], w1.v[2 * q], w1.v[2 * q + 1]);
+                        }
+                        if (r0 + b == 0) {
+                            a0 = w0;
+                            a1 = w1;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                a0.v[e] = __fadd_rn(a0.v[e], w0.v[e]);
+                                a1.v[e] = __fadd_rn(a1.v[e], w1.v[e]);
                             }
                         }
                     }
                 }
             }
-        }
-        if (grp == 0) {
-            t0 = a0;
-            t1 = a1;
-        } else {
+            if (grp == 0) {
+                t0 = a0;
+                t1 = a1;
+            } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                t0.v[e] = __fadd_rn(t0.v[e], a0.v[e]);
-                t1.v[e] = __fadd_rn(t1.v[e], a1.v[e]);
+                for (int e = 0; e < 8; ++e) {
+                    t0.v[e] = __fadd_rn(t0.v[e], a0.v[e]);
+                    t1.v[e] = __fadd_rn(t1.v[e], a1.v[e]);
+                }
             }
         }
-    }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        t0.v[e] = __fdiv_rn(t0.v[e], fW);
-        t1.v[e] = __fdiv_rn(t1.v[e], fW);
-        if (BF16) {
-            t0.v[e] = round_bf16(t0.v[e]);
-            t1.v[e] = round_bf16(t1.v[e]);
+        for (int e = 0; e < 8; ++e) {
+            t0.v[e] = __fdiv_rn(t0.v[e], fW);
+            t1.v[e] = __fdiv_rn(t1.v[e], fW);
         }
+        out0 = t0;
+        out1 = t1;
     }
-    out0 = t0;
-    out1 = t1;
 }
 
 // Optional unscale / accumulation / non-finite check of eight results.

@@ -60,6 +60,53 @@ def test_bf16_reduction(name):
     H.run_full(workloads.get(name).with_(reduce_dtype="bf16"))
 
 
+def _finite_bf16_patterns(rng, n):
+    b = rng.integers(0, 1 << 16, n, dtype=np.uint32).astype(np.uint16)
+    b[(b & 0x7F80) == 0x7F80] &= 0xBFFF          # exponent 0xFF -> 0x7F: finite
+    return b
+
+
+@pytest.mark.parametrize("grad_dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("N", [2, 3, 8])
+@pytest.mark.parametrize("fused", [False, True])
+def test_bf16_reduction_on_every_exponent(grad_dtype, N, fused):
+    """bf16 reduction of gradients drawn from every bf16 exponent (subnormals,
+    zeros of both signs, the largest finite values, sums that overflow) and of
+    rank pairs whose exponents differ by 0..20, so that partial sums fall on
+    and near bf16 rounding midpoints; fp32 gradients also carry random low
+    halves that the input rounding must handle.  The gradient shard must equal
+    the oracle's bit for bit, through the plain and the fused kernels."""
+    rng = np.random.default_rng(1000 * N + (grad_dtype == "f32"))
+    P = 3 * 8192 + 37                             # several tiles and a ragged tail
+    pats = [_finite_bf16_patterns(rng, P) for _ in range(N)]
+    e0 = (pats[0] >> 7) & 0xFF
+    gap = rng.integers(0, 21, P).astype(np.uint16)
+    near = (e0 > 21) & (rng.random(P) < 0.5)
+    pats[1] = np.where(near, (pats[1] & 0x807F) | ((e0 - gap) << 7), pats[1]).astype(np.uint16)
+    if grad_dtype == "f32":
+        low = rng.integers(0, 1 << 16, (N, P), dtype=np.uint32)
+        host = [(p.astype(np.uint32) << 16 | lo).view(np.float32) for p, lo in zip(pats, low)]
+        host = [np.where(np.isfinite(h), h, np.float32(1.5)) for h in host]
+        grads = [torch.from_numpy(h).cuda() for h in host]
+    else:
+        host = pats
+        grads = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).cuda() for h in host]
+    with np.errstate(over="ignore", invalid="ignore"):
+        want = O.reduce_full_bf16(host)
+    u = B.Unit([(P,)], "flat", N, grad_dtype, reduce_dtype="bf16", fuse_reduce_adamw=fused)
+    try:
+        u.load([torch.zeros(P, device="cuda")])
+        if fused:
+            out = torch.empty(P, dtype=torch.int16, device="cuda")
+            u.step(grads, out, dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01))
+        else:
+            u.reduce_scatter(grads)
+        torch.cuda.synchronize()
+        H.assert_bits_equal(u.read_global("grad").cpu().numpy(), want, f"bf16 reduction N={N}")
+    finally:
+        u.close()
+
+
 @pytest.mark.parametrize("name", ["ragged_mini_flat_n7", "ragged_mini_dim0_n64", "gpt_mini_flat_bf16"])
 def test_gather_from_shadow(name):
     H.run_full(workloads.get(name).with_(gather_source="shadow"))
