@@ -79,6 +79,15 @@ class RSOptions(ctypes.Structure):
                 ("found_nonfinite_dev", ctypes.c_void_p)]
 
 
+_ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p)
+_FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p)
+
+
+class Allocator(ctypes.Structure):
+    """fsdp_allocator: alloc(bytes, ctx) -> device pointer or NULL; free(ptr, ctx)."""
+    _fields_ = [("alloc", _ALLOC_FN), ("free", _FREE_FN), ("ctx", ctypes.c_void_p)]
+
+
 class FsdpError(RuntimeError):
     def __init__(self, code: int, where: str, detail: str):
         super().__init__(f"{where}: {detail} (code {code})")
@@ -94,6 +103,8 @@ _PI = ctypes.POINTER(ctypes.c_int)
 _SIGNATURES = {
     "fsdp_plan_layout": (_I, [_I, _PI, _PI64, _I, _I, _PI64, _PI64, ctypes.POINTER(Segment), _I64]),
     "fsdp_unit_create": (_I, [_I, _PI, _PI64, ctypes.POINTER(UnitConfig), ctypes.POINTER(_P)]),
+    "fsdp_unit_create_with_allocator": (_I, [_I, _PI, _PI64, ctypes.POINTER(UnitConfig),
+                                             ctypes.POINTER(Allocator), ctypes.POINTER(_P)]),
     "fsdp_unit_destroy": (_I, [_P]),
     "fsdp_load_params": (_I, [_P, ctypes.POINTER(_P), _P]),
     "fsdp_allgather": (_I, [_P, _P, _P]),
@@ -189,16 +200,66 @@ def fsdp_plan_layout(shapes, layout, num_ranks):
     return P.value, list(segs)[:ns.value]
 
 
+def _unit_config(layout, num_ranks, grad_dtype, reshard_after_forward, replicas, reduce_dtype,
+                 gather_source, fuse_reduce_adamw) -> UnitConfig:
+    return UnitConfig(LAYOUTS.get(layout, layout), int(num_ranks), GRAD_DTYPES.get(grad_dtype, grad_dtype),
+                      1 if reshard_after_forward else 0, int(replicas),
+                      GRAD_DTYPES.get(reduce_dtype, reduce_dtype), GATHER_SOURCES.get(gather_source, gather_source),
+                      1 if fuse_reduce_adamw else 0)
+
+
 def fsdp_unit_create(shapes, layout, num_ranks, grad_dtype="f32", reshard_after_forward=True,
                      replicas=1, reduce_dtype="f32", gather_source="master", fuse_reduce_adamw=False):
     n, nd, dims = _shape_args(shapes)
-    cfg = UnitConfig(LAYOUTS.get(layout, layout), int(num_ranks), GRAD_DTYPES.get(grad_dtype, grad_dtype),
-                     1 if reshard_after_forward else 0, int(replicas),
-                     GRAD_DTYPES.get(reduce_dtype, reduce_dtype), GATHER_SOURCES.get(gather_source, gather_source),
-                     1 if fuse_reduce_adamw else 0)
+    cfg = _unit_config(layout, num_ranks, grad_dtype, reshard_after_forward, replicas, reduce_dtype,
+                       gather_source, fuse_reduce_adamw)
     h = _P()
     _check(lib().fsdp_unit_create(n, nd, dims, ctypes.byref(cfg), ctypes.byref(h)), "fsdp_unit_create")
     return h
+
+
+def fsdp_unit_create_with_allocator(shapes, layout, num_ranks, allocator: Allocator, grad_dtype="f32",
+                                    reshard_after_forward=True, replicas=1, reduce_dtype="f32",
+                                    gather_source="master", fuse_reduce_adamw=False):
+    """`allocator` is an ``Allocator`` struct; the caller keeps it (and the
+    callbacks it holds) alive until the unit is destroyed."""
+    n, nd, dims = _shape_args(shapes)
+    cfg = _unit_config(layout, num_ranks, grad_dtype, reshard_after_forward, replicas, reduce_dtype,
+                       gather_source, fuse_reduce_adamw)
+    h = _P()
+    _check(lib().fsdp_unit_create_with_allocator(n, nd, dims, ctypes.byref(cfg), ctypes.byref(allocator),
+                                                 ctypes.byref(h)), "fsdp_unit_create_with_allocator")
+    return h
+
+
+class TorchAllocator:
+    """Device memory for units from torch's caching allocator: each block is a
+    torch uint8 tensor on the current device (torch aligns blocks to 512
+    bytes), so torch.cuda.memory_allocated() counts the units' arenas and the
+    memory returns to torch's pool when a unit is destroyed.  Keep this object
+    alive while any unit made with it exists.  ``allocs`` / ``frees`` count the
+    calls; ``live`` holds the blocks not yet freed."""
+
+    def __init__(self):
+        self.live = {}
+        self.allocs = 0
+        self.frees = 0
+
+        def _alloc(nbytes, ctx):
+            try:
+                t = torch.empty(int(nbytes), dtype=torch.uint8, device="cuda")
+            except RuntimeError:                  # out of memory: the library reports FSDP_E_OOM
+                return None
+            self.live[t.data_ptr()] = t
+            self.allocs += 1
+            return t.data_ptr()
+
+        def _free(ptr, ctx):
+            self.live.pop(ptr, None)
+            self.frees += 1
+
+        self._callbacks = (_ALLOC_FN(_alloc), _FREE_FN(_free))
+        self.struct = Allocator(self._callbacks[0], self._callbacks[1], None)
 
 
 def fsdp_unit_destroy(h) -> None:
@@ -407,10 +468,19 @@ class Unit:
     """Owns one ``fsdp_unit`` handle; methods call the C entry points."""
 
     def __init__(self, shapes, layout="flat", num_ranks=1, grad_dtype="f32", reshard_after_forward=True,
-                 replicas=1, reduce_dtype="f32", gather_source="master", fuse_reduce_adamw=False):
+                 replicas=1, reduce_dtype="f32", gather_source="master", fuse_reduce_adamw=False,
+                 allocator=None):
+        """`allocator`: None (the library's cudaMalloc) or an object with an
+        ``Allocator`` in its ``struct`` attribute, e.g. ``TorchAllocator()``."""
         self.shapes = [tuple(int(d) for d in s) for s in shapes]
-        self.handle = fsdp_unit_create(self.shapes, layout, num_ranks, grad_dtype, reshard_after_forward,
-                                       replicas, reduce_dtype, gather_source, fuse_reduce_adamw)
+        self.allocator = allocator
+        if allocator is None:
+            self.handle = fsdp_unit_create(self.shapes, layout, num_ranks, grad_dtype, reshard_after_forward,
+                                           replicas, reduce_dtype, gather_source, fuse_reduce_adamw)
+        else:
+            self.handle = fsdp_unit_create_with_allocator(self.shapes, layout, num_ranks, allocator.struct,
+                                                          grad_dtype, reshard_after_forward, replicas,
+                                                          reduce_dtype, gather_source, fuse_reduce_adamw)
         info = fsdp_unit_info(self.handle)
         self.numel = info["numel"]
         self.N = info["num_ranks"]

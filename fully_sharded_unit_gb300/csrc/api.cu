@@ -71,6 +71,7 @@ struct fsdp_unit {
     int reduce_dtype = FSDP_DTYPE_F32;
     int gather_source = FSDP_GATHER_FROM_MASTER;
     int fuse = 0;
+    fsdp_allocator allocator{nullptr, nullptr, nullptr};   // alloc == nullptr: cudaMalloc / cudaFree
     // device-step mode (CUDA-graph replay of AdamW): constants of steps
     // step_base+1 .. step_base+step_count live in step_table; step_counter
     // counts the steps taken on the device since the table was made
@@ -99,6 +100,39 @@ struct fsdp_unit {
 
 namespace {
 
+// Device memory of a unit: from the caller's allocator when one was given,
+// else cudaMalloc.  The buffers are read with 32-byte vector accesses, so a
+// caller's block must be aligned to 256 bytes; a misaligned one is handed
+// back at once.  Returns FSDP_OK or an error code (set via fail()).
+int dev_alloc(fsdp_unit* u, void** p, size_t bytes) {
+    if (bytes == 0) bytes = 32;
+    *p = nullptr;
+    if (u->allocator.alloc != nullptr) {
+        void* q = u->allocator.alloc(bytes, u->allocator.ctx);
+        if (q == nullptr) return fail(FSDP_E_OOM, "the caller's allocator returned NULL");
+        if ((reinterpret_cast<uintptr_t>(q) & 255u) != 0) {
+            u->allocator.free(q, u->allocator.ctx);
+            return fail(FSDP_E_ALIGN, "the caller's allocator returned a block not aligned to 256 bytes");
+        }
+        *p = q;
+        return FSDP_OK;
+    }
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        return fail(e == cudaErrorMemoryAllocation ? FSDP_E_OOM : FSDP_E_CUDA,
+                    std::string("cudaMalloc: ") + cudaGetErrorString(e));
+    }
+    return FSDP_OK;
+}
+
+void dev_free(fsdp_unit* u, void* p) {
+    if (p == nullptr) return;
+    if (u->allocator.alloc != nullptr) u->allocator.free(p, u->allocator.ctx);
+    else cudaFree(p);
+}
+
 void free_unit(fsdp_unit* u) {
     for (void* p : {static_cast<void*>(u->master), static_cast<void*>(u->grad),
                     static_cast<void*>(u->m), static_cast<void*>(u->v),
@@ -106,7 +140,7 @@ void free_unit(fsdp_unit* u) {
                     static_cast<void*>(u->load_tiles), static_cast<void*>(u->param_src),
                     static_cast<void*>(u->step_table), static_cast<void*>(u->step_counter),
                     static_cast<void*>(u->step_status)}) {
-        if (p) cudaFree(p);
+        dev_free(u, p);
     }
     for (auto& r : u->prof) {
         cudaEventDestroy(r.start);
@@ -360,8 +394,16 @@ int fsdp_plan_layout(int nparams, const int* ndims, const int64_t* dims, int lay
 
 int fsdp_unit_create(int nparams, const int* ndims, const int64_t* dims,
                      const fsdp_unit_config* cfg, fsdp_unit** out) {
+    return fsdp_unit_create_with_allocator(nparams, ndims, dims, cfg, nullptr, out);
+}
+
+int fsdp_unit_create_with_allocator(int nparams, const int* ndims, const int64_t* dims,
+                                    const fsdp_unit_config* cfg, const fsdp_allocator* alloc,
+                                    fsdp_unit** out) {
     if (out == nullptr || cfg == nullptr) return fail(FSDP_E_INVALID_ARG, "cfg/out is null");
     *out = nullptr;
+    if (alloc != nullptr && (alloc->alloc == nullptr || alloc->free == nullptr))
+        return fail(FSDP_E_INVALID_ARG, "an allocator needs both alloc and free");
     if (cfg->grad_dtype != FSDP_DTYPE_F32 && cfg->grad_dtype != FSDP_DTYPE_BF16)
         return fail(FSDP_E_INVALID_ARG, "grad_dtype must be FSDP_DTYPE_F32 or FSDP_DTYPE_BF16");
     if (cfg->reduce_dtype != FSDP_DTYPE_F32 && cfg->reduce_dtype != FSDP_DTYPE_BF16)
@@ -394,6 +436,7 @@ int fsdp_unit_create(int nparams, const int* ndims, const int64_t* dims,
     u->reduce_dtype = cfg->reduce_dtype;
     u->gather_source = cfg->gather_source;
     u->fuse = cfg->fuse_reduce_adamw ? 1 : 0;
+    if (alloc != nullptr) u->allocator = *alloc;
 
     std::vector<Tile> tiles, load_tiles;
     fsdp::build_tiles(u->plan, &tiles);
@@ -416,13 +459,11 @@ int fsdp_unit_create(int nparams, const int* ndims, const int64_t* dims,
         {reinterpret_cast<void**>(&u->param_src), static_cast<size_t>(nparams) * sizeof(fsdp::ParamSrc)},
     };
     for (auto& a : allocs) {
-        cudaError_t e = cudaMalloc(a.p, a.bytes > 0 ? a.bytes : 32);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
+        rc = dev_alloc(u, a.p, a.bytes);
+        if (rc != FSDP_OK) {   // the reason is already recorded
             free_unit(u);
             delete u;
-            return fail(e == cudaErrorMemoryAllocation ? FSDP_E_OOM : FSDP_E_CUDA,
-                        std::string("cudaMalloc: ") + cudaGetErrorString(e));
+            return rc;
         }
     }
     cudaError_t e = cudaSuccess;
@@ -686,17 +727,24 @@ int fsdp_adamw_device_steps(fsdp_unit* u, const fsdp_adamw_hp* hp, int64_t count
     }
     std::vector<fsdp::AdamWConsts> table(static_cast<size_t>(count));
     for (int64_t i = 0; i < count; ++i) table[static_cast<size_t>(i)] = adamw_consts(hp, u->t + 1 + i);
-    cudaError_t e = cudaSuccess;
-    if (u->step_counter == nullptr) e = cudaMalloc(reinterpret_cast<void**>(&u->step_counter), 64);
-    if (e == cudaSuccess && u->step_status == nullptr) e = cudaMalloc(reinterpret_cast<void**>(&u->step_status), 64);
-    if (e == cudaSuccess && u->step_table_cap < count) {
+    if (u->step_counter == nullptr) {
+        rc = dev_alloc(u, reinterpret_cast<void**>(&u->step_counter), 64);
+        if (rc) return rc;
+    }
+    if (u->step_status == nullptr) {
+        rc = dev_alloc(u, reinterpret_cast<void**>(&u->step_status), 64);
+        if (rc) return rc;
+    }
+    if (u->step_table_cap < count) {
         cudaStreamSynchronize(st);   // the old table may still be in use
-        if (u->step_table) cudaFree(u->step_table);
+        dev_free(u, u->step_table);
         u->step_table = nullptr;
         u->step_table_cap = 0;
-        e = cudaMalloc(reinterpret_cast<void**>(&u->step_table), sizeof(fsdp::AdamWConsts) * static_cast<size_t>(count));
-        if (e == cudaSuccess) u->step_table_cap = count;
+        rc = dev_alloc(u, reinterpret_cast<void**>(&u->step_table), sizeof(fsdp::AdamWConsts) * static_cast<size_t>(count));
+        if (rc) return rc;
+        u->step_table_cap = count;
     }
+    cudaError_t e = cudaSuccess;
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(u->step_table, table.data(), sizeof(fsdp::AdamWConsts) * table.size(),
                             cudaMemcpyHostToDevice, st);

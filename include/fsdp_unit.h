@@ -178,6 +178,32 @@ FSDP_API int fsdp_plan_layout(int nparams, const int* ndims, const int64_t* dims
 FSDP_API int fsdp_unit_create(int nparams, const int* ndims, const int64_t* dims,
                      const fsdp_unit_config* cfg, fsdp_unit** out);
 
+/* Optional provider of the unit's device memory, for
+ * fsdp_unit_create_with_allocator (so that, for instance, a framework's
+ * caching allocator owns and accounts for the rank arenas).  alloc(bytes,
+ * ctx) returns a block of device memory on the current device, aligned to at
+ * least 256 bytes, or NULL; free(ptr, ctx) takes back a block alloc returned.
+ * The library calls them on the calling thread from
+ * fsdp_unit_create_with_allocator (every buffer the unit owns),
+ * fsdp_adamw_device_steps (its step table and counters) and
+ * fsdp_unit_destroy (all of them, after the device has synchronised), and on
+ * a failure in those calls for the blocks it already obtained.  The struct is
+ * copied; ctx must stay valid until the unit is destroyed. */
+typedef struct {
+    void* (*alloc)(size_t bytes, void* ctx);
+    void (*free)(void* ptr, void* ctx);
+    void* ctx;
+} fsdp_allocator;
+
+/* fsdp_unit_create with the unit's device memory taken from `alloc` (NULL:
+ * cudaMalloc, as fsdp_unit_create).  Errors besides fsdp_unit_create's:
+ * FSDP_E_INVALID_ARG if alloc or free is NULL; FSDP_E_OOM if alloc returns
+ * NULL; FSDP_E_ALIGN if it returns a block not aligned to 256 bytes (the
+ * block is freed at once).  Every block obtained is freed on failure. */
+FSDP_API int fsdp_unit_create_with_allocator(int nparams, const int* ndims, const int64_t* dims,
+                     const fsdp_unit_config* cfg, const fsdp_allocator* alloc,
+                     fsdp_unit** out);
+
 /* Free everything the unit owns.  Synchronises the unit's device first.
  * NULL is accepted. */
 FSDP_API int fsdp_unit_destroy(fsdp_unit* unit);

@@ -82,7 +82,7 @@ class Comparison:
 
 
 def run_full(wl: workloads.Workload, unit: int = 0, use_step: bool = False, steps: int | None = None,
-             gen_device: str = "cpu") -> Comparison:
+             gen_device: str = "cpu", allocator=None) -> Comparison:
     """Whole-unit comparison, every element, every step."""
     shapes = wl.shapes(unit)
     N, P = wl.N, wl.unit_numel(unit)
@@ -95,7 +95,7 @@ def run_full(wl: workloads.Workload, unit: int = 0, use_step: bool = False, step
     orc.load([p.cpu().numpy() for p in params])
     u = B.Unit(shapes, wl.layout, N, wl.grad_dtype, wl.reshard_after_forward, replicas=wl.replicas,
                reduce_dtype=wl.reduce_dtype, gather_source=wl.gather_source,
-               fuse_reduce_adamw=wl.fuse_reduce_adamw)
+               fuse_reduce_adamw=wl.fuse_reduce_adamw, allocator=allocator)
     try:
         u.load([p.cuda() for p in params])
         del params
