@@ -524,9 +524,14 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_kernel(const Tile* __re
     const float fW = static_cast<float>(a.F * groups);
     const bool post = EXT && (a.scale || a.accumulate);
     int32_t* const found = EXT ? a.found : nullptr;
-    // bf16 gradients: 16-element groups, one 32-byte load per rank (measured
-    // 7.46 TB/s against 7.24 TB/s with 16-byte loads on the minGPT unit)
-    constexpr int A = std::is_same<GT, uint16_t>::value ? 16 : 8;
+    // bf16 gradients, plain reduce-scatter: 16-element groups, one 32-byte
+    // load per rank (measured 7.46 TB/s against 7.24 TB/s with 16-byte loads
+    // on the minGPT unit).  The extended one keeps 8-element groups: its
+    // separate per-group and total accumulators make the 16-wide form need
+    // 128 registers (2 CTAs per SM), the 8-wide one 78 (3 CTAs per SM), which
+    // measured 9.44 ms against 9.73 ms for two replication groups and 6.10 ms
+    // against 6.53 ms per accumulated micro-batch.
+    constexpr int A = (std::is_same<GT, uint16_t>::value && !EXT) ? 16 : 8;
     bool bad = false;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const Tile tl = tiles[t];
