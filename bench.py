@@ -62,6 +62,26 @@ def counted_bytes(wl: workloads.Workload, unit: int) -> dict:
                 gathers=R, h2d=W * gb * P, d2h=2 * P)
 
 
+L2_BYTES = 129e6   # GB300 L2 cache
+
+
+def l2_statement(wl: workloads.Workload) -> str:
+    """How the timed steps stand to the L2 cache (no flush is done).  A unit
+    touches 20 bytes per element (fp32 master, gradient shard, m, v; bf16
+    shadow and gathered output) plus its W gradients."""
+    per_unit = [20 * wl.unit_numel(i) + wl.world * (4 if wl.grad_dtype == "f32" else 2) * wl.unit_numel(i)
+                for i in range(wl.n_units)]
+    smallest_kernel = min(min(counted_bytes(wl, i)["gather"], counted_bytes(wl, i)["reduce_scatter"])
+                          for i in range(wl.n_units))
+    if smallest_kernel > L2_BYTES:
+        return "inputs larger than L2; no flush"
+    if sum(per_unit) > L2_BYTES:
+        return (f"no flush: the step touches {sum(per_unit) / 1e9:.2f} GB over {wl.n_units} units, more than "
+                f"L2, so each unit step starts cold; one unit's buffers ({max(per_unit) / 1e6:.0f} MB) can "
+                "partly stay in L2 between its own kernels")
+    return f"no flush: the whole state ({sum(per_unit) / 1e6:.1f} MB) fits in L2 (L2-resident)"
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -408,7 +428,7 @@ def run_ours(args, world, rank, local):
                    "fused_reduce_adamw": wl.fuse_reduce_adamw, "micro_batches": args.micro_batches,
                    "counted_bytes_per_step": step_bytes,
                    "gather_source": "fp32 master" if wl.gather_source == "master" else "bf16 shadow",
-                   "l2": "inputs larger than L2; no flush", "parallelism": f"replicas x{world}"},
+                   "l2": l2_statement(wl), "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "graph": graph, "fastest_variant": fastest,
         "clocks": clk.result,
