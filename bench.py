@@ -386,6 +386,11 @@ def run_ours(args, world, rank, local):
     value_rank = step_bytes * args.steps / (ms * 1e-3) / 1e9
     value = world * step_bytes * args.steps / (ms_max * 1e-3) / 1e9
 
+    # the same configuration without the profiler's event pair around every
+    # launch (which serialises consecutive kernels): the step as a caller runs it
+    unprofiled = run_variant(args, units, step, stream, hp, world, dev, wl)
+    del unprofiled["gather_source"], unprofiled["fused_reduce_adamw"]
+
     # the fastest configuration on the same units: bf16-shadow gather and the
     # fused reduce-scatter + AdamW (identical results, fewer bytes)
     fastest = None
@@ -430,7 +435,7 @@ def run_ours(args, world, rank, local):
                    "gather_source": "fp32 master" if wl.gather_source == "master" else "bf16 shadow",
                    "l2": l2_statement(wl), "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "graph": graph, "fastest_variant": fastest,
+        "graph": graph, "unprofiled": unprofiled, "fastest_variant": fastest,
         "clocks": clk.result,
     }
     print(json.dumps(line), flush=True)

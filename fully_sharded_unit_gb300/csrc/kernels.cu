@@ -13,6 +13,11 @@
 // aligned in the arena.  Each tile has at most A-1 unaligned head and A-1
 // tail elements (A = 8 or 16), done scalar.
 //
+// Launch: every kernel is launched with programmatic stream serialization
+// and starts with griddepcontrol.wait (pdl_enter), so the next kernel's CTAs
+// are scheduled during the previous kernel's last wave while the stream order
+// of every memory access stays the same.
+//
 // Numerics: every floating-point operation is an explicitly rounded
 // intrinsic (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so nothing is
 // contracted into FMAs and the results equal a sequential IEEE evaluation of
@@ -114,6 +119,18 @@ __device__ __forceinline__ void widen2(uint32_t w, float& lo, float& hi) {
     hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
+// Programmatic dependent launch.  Every kernel is launched with programmatic
+// stream serialization, so its grid may be scheduled while the previous
+// kernel of the stream is still running; it waits here, before touching any
+// memory, until that kernel has completed and its writes are visible, so the
+// stream order of all reads and writes is unchanged.  Having waited, it lets
+// the next kernel's grid be scheduled in turn: its CTAs take the SMs that
+// this grid's last wave leaves idle and start the moment this grid ends.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Correctly rounded (RNE) addition of two bf16 pairs.  It equals the fp32 sum
 // rounded once to bf16: the exact sum of two bf16 values rounded to fp32 and
 // then to bf16 cannot differ from it rounded straight to bf16, because fp32
@@ -154,6 +171,7 @@ __global__ void __launch_bounds__(kBlock) shard_in_kernel(const Tile* __restrict
                                                           const ParamSrc* __restrict__ params,
                                                           float* __restrict__ master,
                                                           uint16_t* __restrict__ shadow) {
+    pdl_enter();
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const Tile tl = tiles[t];
         const ParamSrc ps = params[tl.aux];
@@ -172,6 +190,7 @@ __global__ void __launch_bounds__(kBlock) gather_cast_kernel(const Tile* __restr
                                                              int64_t ntiles,
                                                              const float* __restrict__ master,
                                                              uint16_t* __restrict__ out) {
+    pdl_enter();
     const int tid = threadIdx.x;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const Tile tl = tiles[t];
@@ -204,6 +223,7 @@ __global__ void __launch_bounds__(kBlock) gather_shadow_kernel(const Tile* __res
                                                                int64_t ntiles,
                                                                const uint16_t* __restrict__ shadow,
                                                                uint16_t* __restrict__ out) {
+    pdl_enter();
     const int tid = threadIdx.x;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const Tile tl = tiles[t];
@@ -235,6 +255,7 @@ __global__ void __launch_bounds__(kBlock) gather_shadow_kernel(const Tile* __res
 __global__ void __launch_bounds__(kBlock) cast_range_kernel(const float* __restrict__ master,
                                                             uint16_t* __restrict__ shadow,
                                                             int64_t n8) {
+    pdl_enter();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; i < n8; i += stride)
         st8bf(shadow + 8 * i, pack8(ld8_ro(master + 8 * i)));
@@ -519,6 +540,7 @@ template <typename GT, int NMAX, bool BF16, bool EXT>
 __global__ void __launch_bounds__(kBlock) reduce_scatter_kernel(const Tile* __restrict__ tiles,
                                                                 int64_t ntiles, GradPtrs<NMAX> gp,
                                                                 ReduceArgs a, float* __restrict__ gshard) {
+    pdl_enter();
     const int tid = threadIdx.x;
     const int groups = EXT ? a.groups : 1;
     const float fW = static_cast<float>(a.F * groups);
@@ -601,6 +623,7 @@ __device__ __forceinline__ bool step_constants(const StepSource& src, AdamWConst
 }
 
 __global__ void advance_step_kernel(int64_t* counter, int64_t count) {
+    pdl_enter();
     if (*counter < count) *counter += 1;
 }
 
@@ -610,6 +633,7 @@ __global__ void __launch_bounds__(kBlock) adamw_kernel(int64_t n8, float* __rest
                                                        float* __restrict__ v,
                                                        uint16_t* __restrict__ shadow,
                                                        StepSource src) {
+    pdl_enter();
     AdamWConsts c;
     if (!step_constants(src, c)) return;   // uniform over the grid
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
@@ -648,6 +672,7 @@ __global__ void __launch_bounds__(kBlock, sizeof(GT) == 2 ? 3 : 2) reduce_adamw_
                                                               float* __restrict__ p, float* __restrict__ m,
                                                               float* __restrict__ v,
                                                               uint16_t* __restrict__ shadow, StepSource src) {
+    pdl_enter();
     AdamWConsts c;
     if (!step_constants(src, c)) return;   // uniform over the grid
     __shared__ __align__(16) float gsm[kTile];
@@ -718,34 +743,49 @@ unsigned grid_for(int64_t work) {
     return static_cast<unsigned>(work < cap ? work : cap);
 }
 
+// Launch `kernel` on `grid` CTAs of `block` threads with programmatic stream
+// serialization (see pdl_enter).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace
 
 cudaError_t launch_shard_in(const Tile* tiles, int64_t ntiles, const ParamSrc* params,
                             float* master, uint16_t* shadow, cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
-    shard_in_kernel<<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, params, master, shadow);
-    return cudaGetLastError();
+    return launch_pdl(shard_in_kernel, grid_for(ntiles), kBlock, st, tiles, ntiles, params, master,
+                      shadow);
 }
 
 cudaError_t launch_gather(const Tile* tiles, int64_t ntiles, const float* master, uint16_t* out, cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
-    gather_cast_kernel<<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, master, out);
-    return cudaGetLastError();
+    return launch_pdl(gather_cast_kernel, grid_for(ntiles), kBlock, st, tiles, ntiles, master, out);
 }
 
 cudaError_t launch_gather_shadow(const Tile* tiles, int64_t ntiles, const uint16_t* shadow,
                                  uint16_t* out, cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
-    gather_shadow_kernel<<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, shadow, out);
-    return cudaGetLastError();
+    return launch_pdl(gather_shadow_kernel, grid_for(ntiles), kBlock, st, tiles, ntiles, shadow, out);
 }
 
 cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t begin, int64_t n, cudaStream_t st) {
     const int64_t n8 = n / 8;
     if (n8 == 0) return cudaSuccess;
-    cast_range_kernel<<<grid_for((n8 + kBlock - 1) / kBlock), kBlock, 0, st>>>(
-        master + begin, shadow + begin, n8);
-    return cudaGetLastError();
+    return launch_pdl(cast_range_kernel, grid_for((n8 + kBlock - 1) / kBlock), kBlock, st, master + begin,
+                      shadow + begin, n8);
 }
 
 template <typename GT, int NMAX, bool BF16, bool EXT>
@@ -754,9 +794,8 @@ static cudaError_t launch_rs_t(const Tile* tiles, int64_t ntiles, const void* co
     GradPtrs<NMAX> gp;
     const int W = a.F * a.groups;
     for (int r = 0; r < NMAX; ++r) gp.p[r] = r < W ? grads[r] : nullptr;
-    reduce_scatter_kernel<GT, NMAX, BF16, EXT>
-        <<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, gp, a, gshard);
-    return cudaGetLastError();
+    return launch_pdl(reduce_scatter_kernel<GT, NMAX, BF16, EXT>, grid_for(ntiles), kBlock, st, tiles, ntiles,
+                      gp, a, gshard);
 }
 
 template <typename GT, int NMAX, bool BF16>
@@ -793,12 +832,10 @@ static cudaError_t launch_ra_t(const Tile* tiles, int64_t ntiles, const void* co
     const int W = a.F * a.groups;
     for (int r = 0; r < NMAX; ++r) gp.p[r] = r < W ? grads[r] : nullptr;
     if (a.groups > 1)
-        reduce_adamw_kernel<GT, NMAX, BF16, true>
-            <<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, gp, a, gshard, p, m, v, shadow, c);
-    else
-        reduce_adamw_kernel<GT, NMAX, BF16, false>
-            <<<grid_for(ntiles), kBlock, 0, st>>>(tiles, ntiles, gp, a, gshard, p, m, v, shadow, c);
-    return cudaGetLastError();
+        return launch_pdl(reduce_adamw_kernel<GT, NMAX, BF16, true>, grid_for(ntiles), kBlock, st, tiles,
+                          ntiles, gp, a, gshard, p, m, v, shadow, c);
+    return launch_pdl(reduce_adamw_kernel<GT, NMAX, BF16, false>, grid_for(ntiles), kBlock, st, tiles,
+                      ntiles, gp, a, gshard, p, m, v, shadow, c);
 }
 
 template <typename GT>
@@ -825,13 +862,12 @@ cudaError_t launch_reduce_adamw(const Tile* tiles, int64_t ntiles, const void* c
 cudaError_t launch_adamw(int64_t n8, float* p, const float* g, float* m, float* v,
                          uint16_t* shadow, const StepSource& c, cudaStream_t st) {
     if (n8 == 0) return cudaSuccess;
-    adamw_kernel<<<grid_for((n8 + kBlock - 1) / kBlock), kBlock, 0, st>>>(n8, p, g, m, v, shadow, c);
-    return cudaGetLastError();
+    return launch_pdl(adamw_kernel, grid_for((n8 + kBlock - 1) / kBlock), kBlock, st, n8, p, g, m, v, shadow,
+                      c);
 }
 
 cudaError_t launch_advance_step(int64_t* counter, int64_t count, cudaStream_t st) {
-    advance_step_kernel<<<1, 1, 0, st>>>(counter, count);
-    return cudaGetLastError();
+    return launch_pdl(advance_step_kernel, 1, 1, st, counter, count);
 }
 
 }  // namespace fsdp
