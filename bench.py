@@ -416,7 +416,10 @@ def run_ours(args, world, rank, local):
                "sample": f"3 oracle unit steps on one FLAT unit of {S} elements drawn like {wl.name} "
                          f"(N={wl.N}, {wl.grad_dtype} grads)", "host_cores_available": cpu_cores_info()}
 
+    # FSDP_KSTATUS_* bits raised by any kernel during the run (0: none)
+    kstatus = 0
     for u in units:
+        kstatus |= u.kernel_status(stream)
         u.close()
     if rank != 0:
         return
@@ -435,7 +438,7 @@ def run_ours(args, world, rank, local):
                    "gather_source": "fp32 master" if wl.gather_source == "master" else "bf16 shadow",
                    "l2": l2_statement(wl), "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "graph": graph, "unprofiled": unprofiled, "fastest_variant": fastest,
+        "graph": graph, "unprofiled": unprofiled, "fastest_variant": fastest, "kernel_status": kstatus,
         "clocks": clk.result,
     }
     print(json.dumps(line), flush=True)

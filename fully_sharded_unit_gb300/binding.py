@@ -47,6 +47,8 @@ FSDP_KERNEL_ADAMW = 3
 FSDP_KERNEL_REDUCE_ADAMW = 4
 FSDP_KERNEL_COUNT = 5
 
+FSDP_KSTATUS_WAIT_TIMEOUT = 1
+
 LAYOUTS = {"flat": FSDP_LAYOUT_FLAT, "dim0": FSDP_LAYOUT_DIM0, "flat_padded": FSDP_LAYOUT_FLAT_PADDED}
 GRAD_DTYPES = {"f32": FSDP_DTYPE_F32, "bf16": FSDP_DTYPE_BF16}
 GATHER_SOURCES = {"master": FSDP_GATHER_FROM_MASTER, "shadow": FSDP_GATHER_FROM_SHADOW}
@@ -128,6 +130,8 @@ _SIGNATURES = {
     "fsdp_profile_enable": (_I, [_P, _I]),
     "fsdp_profile_read": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), _PI64]),
     "fsdp_profile_reset": (_I, [_P]),
+    "fsdp_kernel_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
+    "fsdp_selftest_bounded_wait": (_I, [ctypes.c_double, ctypes.POINTER(ctypes.c_int32), _P]),
     "fsdp_host_device_pointer": (_I, [_P, ctypes.POINTER(_P)]),
     "fsdp_strerror": (ctypes.c_char_p, [_I]),
     "fsdp_last_error": (ctypes.c_char_p, []),
@@ -412,6 +416,21 @@ def fsdp_memory_report(h, rank):
     return dict(zip(("param", "grad", "adam", "shadow", "pad"), (v.value for v in vals)))
 
 
+def fsdp_kernel_status(h, stream=None) -> int:
+    """FSDP_KSTATUS_* bits raised since the last call (0: none); clears them."""
+    f = ctypes.c_int32()
+    _check(lib().fsdp_kernel_status(h, ctypes.byref(f), _stream(stream)), "fsdp_kernel_status")
+    return f.value
+
+
+def fsdp_selftest_bounded_wait(limit_seconds=0.05, stream=None) -> bool:
+    """True when a wait that nothing completes ran out and reported it."""
+    t = ctypes.c_int32()
+    _check(lib().fsdp_selftest_bounded_wait(float(limit_seconds), ctypes.byref(t), _stream(stream)),
+           "fsdp_selftest_bounded_wait")
+    return bool(t.value)
+
+
 def fsdp_profile_enable(h, on=True) -> None:
     _check(lib().fsdp_profile_enable(h, 1 if on else 0), "fsdp_profile_enable")
 
@@ -566,3 +585,6 @@ class Unit:
 
     def memory_report(self, rank):
         return fsdp_memory_report(self.handle, rank)
+
+    def kernel_status(self, stream=None) -> int:
+        return fsdp_kernel_status(self.handle, stream)

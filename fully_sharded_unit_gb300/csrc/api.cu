@@ -82,6 +82,7 @@ struct fsdp_unit {
     int64_t step_base = 0;
     int64_t* step_counter = nullptr;
     int32_t* step_status = nullptr;
+    int32_t* kstatus = nullptr;   // FSDP_KSTATUS_* bits raised by kernels
     float* master = nullptr;
     float* grad = nullptr;
     float* m = nullptr;
@@ -139,7 +140,7 @@ void free_unit(fsdp_unit* u) {
                     static_cast<void*>(u->shadow), static_cast<void*>(u->tiles),
                     static_cast<void*>(u->load_tiles), static_cast<void*>(u->param_src),
                     static_cast<void*>(u->step_table), static_cast<void*>(u->step_counter),
-                    static_cast<void*>(u->step_status)}) {
+                    static_cast<void*>(u->step_status), static_cast<void*>(u->kstatus)}) {
         dev_free(u, p);
     }
     for (auto& r : u->prof) {
@@ -321,7 +322,7 @@ int enqueue_reduce_adamw(fsdp_unit* u, const void* const* grads, const fsdp_adam
     const fsdp::StepSource c = step_source(u, hp);
     int rc = profiled_launch(u, FSDP_KERNEL_REDUCE_ADAMW, st, "fused reduce-scatter + AdamW launch", [&] {
         return fsdp::launch_reduce_adamw(u->tiles, u->ntiles, grads, u->grad_dtype, a, u->grad, u->master,
-                                         u->m, u->v, u->shadow, c, st);
+                                         u->m, u->v, u->shadow, c, u->kstatus, st);
     });
     if (rc == FSDP_OK) rc = advance_device_step(u, st);
     if (rc == FSDP_OK) u->t += 1;
@@ -356,6 +357,42 @@ const char* fsdp_strerror(int code) {
 }
 
 const char* fsdp_last_error(void) { return g_last_error.c_str(); }
+
+int fsdp_kernel_status(fsdp_unit* u, int32_t* flags, void* stream) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    if (flags == nullptr) return fail(FSDP_E_INVALID_ARG, "flags is null");
+    DeviceGuard dg(u->device);
+    if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, u->kstatus, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(u->kstatus, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the kernel status word");
+    *flags = v;
+    return FSDP_OK;
+}
+
+int fsdp_selftest_bounded_wait(double limit_seconds, int32_t* timed_out, void* stream) {
+    if (timed_out == nullptr) return fail(FSDP_E_INVALID_ARG, "timed_out is null");
+    if (!(limit_seconds >= 1e-3 && limit_seconds <= 10.0))
+        return fail(FSDP_E_INVALID_ARG, "limit_seconds must be in [1e-3, 10]");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t* word = nullptr;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&word), sizeof(int32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "self-test status word");
+    int32_t v = 0;
+    e = cudaMemsetAsync(word, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess)
+        e = fsdp::launch_wait_selftest(word, static_cast<unsigned long long>(limit_seconds * 1e9), st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&v, word, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    cudaFree(word);
+    if (e != cudaSuccess) return cuda_fail(e, "bounded-wait self-test");
+    *timed_out = (v & FSDP_KSTATUS_WAIT_TIMEOUT) ? 1 : 0;
+    return FSDP_OK;
+}
 
 int fsdp_host_device_pointer(const void* host, void** dev) {
     if (host == nullptr || dev == nullptr) return fail(FSDP_E_INVALID_ARG, "host/dev is null");
@@ -457,6 +494,7 @@ int fsdp_unit_create_with_allocator(int nparams, const int* ndims, const int64_t
         {reinterpret_cast<void**>(&u->tiles), tiles.size() * sizeof(Tile)},
         {reinterpret_cast<void**>(&u->load_tiles), load_tiles.size() * sizeof(Tile)},
         {reinterpret_cast<void**>(&u->param_src), static_cast<size_t>(nparams) * sizeof(fsdp::ParamSrc)},
+        {reinterpret_cast<void**>(&u->kstatus), 32},
     };
     for (auto& a : allocs) {
         rc = dev_alloc(u, a.p, a.bytes);
@@ -468,6 +506,7 @@ int fsdp_unit_create_with_allocator(int nparams, const int* ndims, const int64_t
     }
     cudaError_t e = cudaSuccess;
     for (int i = 0; i < 5 && e == cudaSuccess; ++i) e = cudaMemset(*allocs[i].p, 0, allocs[i].bytes);
+    if (e == cudaSuccess) e = cudaMemset(u->kstatus, 0, 32);
     if (e == cudaSuccess && !tiles.empty())
         e = cudaMemcpy(u->tiles, tiles.data(), tiles.size() * sizeof(Tile), cudaMemcpyHostToDevice);
     if (e == cudaSuccess && !load_tiles.empty())

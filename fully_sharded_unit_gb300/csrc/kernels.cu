@@ -730,6 +730,309 @@ __global__ void __launch_bounds__(kBlock, sizeof(GT) == 2 ? 3 : 2) reduce_adamw_
     }
 }
 
+// ---------------------------------------------------------------- fused reduce-scatter + AdamW, bulk-copy staged
+
+// The fused reduce-scatter + AdamW with its inputs staged in shared memory.
+// A CTA takes one tile and streams it in chunks of kChunk elements through a
+// ring of kStages stages.  A stage holds the chunk's W gradient rows and its
+// p, m, v; one thread brings them in with bulk asynchronous copies
+// (cp.async.bulk, the tensor-memory accelerator's untiled form) counted by the
+// stage's mbarrier, and all threads fold, update and store from shared
+// memory.  The loads in flight live in shared memory instead of registers:
+// 60 registers and no spills against 80 with spills for the register-staged
+// kernel, 7.12 TB/s against 6.74 TB/s on the minGPT unit (bf16 gradients,
+// W = 8).  Measured over chunk x stages: 2048 x 2 (115 KB, 2 CTAs per SM) and
+// 1024 x 3 (86 KB, 2 per SM) within 0.4 %; 512-element chunks (1 KB copies)
+// and 2048 x 3 (1 CTA per SM) 10-35 % slower; one CTA per tile beats 2 or 4
+// tiles per CTA and a persistent grid.  Used when W x gradient bytes <= 16
+// (stage <= 56 KB); wider units take reduce_adamw_kernel.
+constexpr int kChunk = 2048;
+constexpr int kStages = 2;
+constexpr int kBulkMaxRowBytes = 16;   // W * sizeof(GT) limit for the staged kernel
+// A wait on a stage gives up after this long: the kernel then raises bit
+// FSDP_KSTATUS_WAIT_TIMEOUT of the unit's status word, waits (again bounded)
+// for its own copies in flight and returns.
+constexpr unsigned long long kWaitLimitNs = 10000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the barrier phase with the given parity; false if it has not
+// completed within limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
+    const uint32_t addr = smem_addr(bar);
+    unsigned long long t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (i == 0) t0 = global_ns();
+        else if ((i & 63) == 0 && global_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Layout of one stage: W gradient rows of kChunk GT, then p, m, v (fp32).
+template <typename GT>
+__device__ __forceinline__ size_t stage_bytes(int W) {
+    return static_cast<size_t>(kChunk) * (W * sizeof(GT) + 12);
+}
+
+// The aligned body of a tile: [ga, gb), multiples of 16 elements.
+struct Body {
+    int64_t ga;   // global index of the first body element
+    int64_t sa;   // its arena slot
+    int64_t n;    // body elements (multiple of 16)
+    int head;     // elements before ga
+    int tail;     // elements after the body
+};
+
+__device__ __forceinline__ Body tile_body(const Tile& tl) {
+    Body b;
+    const int64_t ga = (tl.g + 15) & ~int64_t(15);
+    const int64_t ge = tl.g + tl.len;
+    int64_t gb = ge & ~int64_t(15);
+    if (gb < ga) gb = ga;
+    if (ga >= ge) {
+        b.ga = ge;
+        b.n = 0;
+        b.head = tl.len;
+        b.tail = 0;
+    } else {
+        b.ga = ga;
+        b.n = gb - ga;
+        b.head = static_cast<int>(ga - tl.g);
+        b.tail = static_cast<int>(ge - gb);
+    }
+    b.sa = tl.s + (b.ga - tl.g);
+    return b;
+}
+
+// Four consecutive reduced gradients from a stage, same operation order as
+// reduce8 (fp32 fold within each group, then across groups, then / W; or
+// the bf16 fold).
+template <typename GT, bool BF16>
+__device__ __forceinline__ void reduce4_smem(const unsigned char* rows, int F, int groups, float fW, int e,
+                                             float out[4]) {
+    if constexpr (BF16) {
+        uint32_t acc[2];
+        for (int r = 0; r < F; ++r) {
+            uint32_t w[2];
+            if constexpr (sizeof(GT) == 2) {
+                const uint2 q = *reinterpret_cast<const uint2*>(rows + (static_cast<size_t>(r) * kChunk + e) * 2);
+                w[0] = q.x;
+                w[1] = q.y;
+            } else {
+                const float4 q = *reinterpret_cast<const float4*>(rows + (static_cast<size_t>(r) * kChunk + e) * 4);
+                w[0] = pack_bf16x2(q.x, q.y);
+                w[1] = pack_bf16x2(q.z, q.w);
+            }
+            acc[0] = r == 0 ? w[0] : add_bf16x2(acc[0], w[0]);
+            acc[1] = r == 0 ? w[1] : add_bf16x2(acc[1], w[1]);
+        }
+        widen2(acc[0], out[0], out[1]);
+        widen2(acc[1], out[2], out[3]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) out[k] = round_bf16(__fdiv_rn(out[k], fW));
+    } else {
+        float tot[4];
+        for (int grp = 0; grp < groups; ++grp) {
+            float acc[4];
+            for (int r = 0; r < F; ++r) {
+                const int row = grp * F + r;
+                float x[4];
+                if constexpr (sizeof(GT) == 2) {
+                    const uint2 q = *reinterpret_cast<const uint2*>(rows + (static_cast<size_t>(row) * kChunk + e) * 2);
+                    widen2(q.x, x[0], x[1]);
+                    widen2(q.y, x[2], x[3]);
+                } else {
+                    const float4 q = *reinterpret_cast<const float4*>(rows + (static_cast<size_t>(row) * kChunk + e) * 4);
+                    x[0] = q.x;
+                    x[1] = q.y;
+                    x[2] = q.z;
+                    x[3] = q.w;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[k] = r == 0 ? x[k] : __fadd_rn(acc[k], x[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) tot[k] = grp == 0 ? acc[k] : __fadd_rn(tot[k], acc[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) out[k] = __fdiv_rn(tot[k], fW);
+    }
+}
+
+template <typename GT, int NMAX, bool BF16, bool HYBRID>
+__global__ void __launch_bounds__(kBlock) reduce_adamw_bulk_kernel(const Tile* __restrict__ tiles,
+                                                                   int64_t ntiles, GradPtrs<NMAX> gp,
+                                                                   ReduceArgs a, float* __restrict__ gshard,
+                                                                   float* __restrict__ p, float* __restrict__ m,
+                                                                   float* __restrict__ v,
+                                                                   uint16_t* __restrict__ shadow, StepSource src,
+                                                                   int32_t* wait_status) {
+    // Waits for the previous kernel like pdl_enter, but does not let the next
+    // kernel's CTAs be scheduled before this grid ends: those early CTAs,
+    // parked beside this kernel's last wave, cost 0.23 ms per launch on the
+    // minGPT unit (27.94 against 27.47 ms per fused two-unit step).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    AdamWConsts c;
+    if (!step_constants(src, c)) return;   // uniform over the grid
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    unsigned char* ring = smem + 128;
+    const int tid = threadIdx.x;
+    const int groups = HYBRID ? a.groups : 1;
+    const int W = a.F * groups;
+    const float fW = static_cast<float>(W);
+    const size_t sbytes = stage_bytes<GT>(W);
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    // producer state (thread 0): the next chunk to bring in
+    int64_t pt = blockIdx.x;   // its tile
+    int64_t pc = 0;            // its chunk within the tile
+    Body pb{};
+    bool pb_valid = false;
+    uint32_t issued = 0, consumed = 0;
+    auto top_up = [&]() {
+        while (issued - consumed < static_cast<uint32_t>(kStages) && pt < ntiles) {
+            if (!pb_valid) {
+                pb = tile_body(tiles[pt]);
+                pb_valid = true;
+            }
+            const int64_t nch = (pb.n + kChunk - 1) / kChunk;
+            if (pc >= nch) {
+                pt += gridDim.x;
+                pc = 0;
+                pb_valid = false;
+                continue;
+            }
+            const int64_t off = pc * kChunk;
+            const uint32_t n = static_cast<uint32_t>(pb.n - off < kChunk ? pb.n - off : kChunk);
+            const int s = static_cast<int>(issued % kStages);
+            unsigned char* st = ring + s * sbytes;
+            mbar_expect_tx(&full[s], n * static_cast<uint32_t>(W * sizeof(GT) + 12));
+            for (int r = 0; r < W; ++r)
+                bulk_g2s(st + static_cast<size_t>(r) * kChunk * sizeof(GT),
+                         static_cast<const GT*>(gp.p[r]) + pb.ga + off, n * sizeof(GT), &full[s]);
+            unsigned char* pmv = st + static_cast<size_t>(W) * kChunk * sizeof(GT);
+            bulk_g2s(pmv, p + pb.sa + off, n * 4, &full[s]);
+            bulk_g2s(pmv + kChunk * 4, m + pb.sa + off, n * 4, &full[s]);
+            bulk_g2s(pmv + 2 * kChunk * 4, v + pb.sa + off, n * 4, &full[s]);
+            ++issued;
+            ++pc;
+        }
+    };
+
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const Tile tl = tiles[t];
+        const Body b = tile_body(tl);
+        // unaligned head and tail, straight from global memory
+        int j = -1;
+        if (tid < b.head) j = tid;
+        else if (tid >= 16 && tid < 16 + b.tail) j = b.head + static_cast<int>(b.n) + (tid - 16);
+        if (j >= 0) {
+            const float xj = reduce1<GT, NMAX, BF16>(gp, a, groups, fW, tl.g + j);
+            const int64_t s = tl.s + j;
+            gshard[s] = xj;
+            float pp = p[s], mm = m[s], vv = v[s];
+            adamw_elem(pp, xj, mm, vv, c);
+            p[s] = pp;
+            m[s] = mm;
+            v[s] = vv;
+            shadow[s] = to_bf16(pp);
+        }
+        const int64_t nch = (b.n + kChunk - 1) / kChunk;
+        for (int64_t ch = 0; ch < nch; ++ch) {
+            if (tid == 0) top_up();
+            const int s = static_cast<int>(consumed % kStages);
+            const uint32_t parity = (consumed / kStages) & 1u;
+            const bool got = mbar_wait(&full[s], parity);
+            const int64_t off = ch * kChunk;
+            const int64_t n = b.n - off < kChunk ? b.n - off : kChunk;
+            for (int e = tid * 4; got && e < n; e += 4 * kBlock) {
+                const unsigned char* st = ring + s * sbytes;
+                float G[4];
+                reduce4_smem<GT, BF16>(st, a.F, groups, fW, e, G);
+                const float* pmv = reinterpret_cast<const float*>(st + static_cast<size_t>(W) * kChunk * sizeof(GT));
+                float4 P = *reinterpret_cast<const float4*>(pmv + e);
+                float4 M = *reinterpret_cast<const float4*>(pmv + kChunk + e);
+                float4 V = *reinterpret_cast<const float4*>(pmv + 2 * kChunk + e);
+                adamw_elem(P.x, G[0], M.x, V.x, c);
+                adamw_elem(P.y, G[1], M.y, V.y, c);
+                adamw_elem(P.z, G[2], M.z, V.z, c);
+                adamw_elem(P.w, G[3], M.w, V.w, c);
+                const int64_t so = b.sa + off + e;
+                *reinterpret_cast<float4*>(gshard + so) = make_float4(G[0], G[1], G[2], G[3]);
+                *reinterpret_cast<float4*>(p + so) = P;
+                *reinterpret_cast<float4*>(m + so) = M;
+                *reinterpret_cast<float4*>(v + so) = V;
+                *reinterpret_cast<uint2*>(shadow + so) = make_uint2(pack_bf16x2(P.x, P.y), pack_bf16x2(P.z, P.w));
+            }
+            ++consumed;
+            ok = __syncthreads_and(got) != 0;
+            if (!ok) break;
+        }
+        if (!ok) break;
+    }
+    if (!ok) {
+        // a copy did not arrive in time: report, wait (bounded) for the copies
+        // this CTA still has in flight, and leave
+        if (tid == 0) {
+            atomicOr(wait_status, FSDP_KSTATUS_WAIT_TIMEOUT);
+            for (uint32_t q = consumed - 1; q < issued; ++q) mbar_wait(&full[q % kStages], (q / kStages) & 1u);
+        }
+        __syncthreads();
+    }
+}
+
+// A bounded wait on a barrier that nothing completes: exercises the limit
+// and the status path of mbar_wait without any copy in flight.
+__global__ void wait_selftest_kernel(int32_t* status, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);   // expects one arrival, which never comes
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const bool got = mbar_wait(&bar, 0, limit_ns);
+    if (__syncthreads_and(got) == 0 && threadIdx.x == 0) atomicOr(status, FSDP_KSTATUS_WAIT_TIMEOUT);
+}
+
 // Grid policy: one CTA per tile (segment kernels) or per 256 groups of 8
 // elements (flat kernels), launched in order, instead of a persistent grid
 // that strides over the work.  Measured on GB300 with the minGPT unit, the
@@ -746,19 +1049,25 @@ unsigned grid_for(int64_t work) {
 // Launch `kernel` on `grid` CTAs of `block` threads with programmatic stream
 // serialization (see pdl_enter).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t st,
-                       Args... args) {
+cudaError_t launch_pdl_smem(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                            cudaStream_t st, Args... args) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t st,
+                       Args... args) {
+    return launch_pdl_smem(kernel, grid, block, 0, st, args...);
 }
 
 }  // namespace
@@ -824,13 +1133,39 @@ cudaError_t launch_reduce_scatter(const Tile* tiles, int64_t ntiles, const void*
     return launch_rs_dt<float>(tiles, ntiles, grads, a, gshard, st);
 }
 
+// The staged kernel needs more than the default 48 KB of dynamic shared
+// memory: raise the kernel's limit once per instantiation.
+template <typename GT, int NMAX, bool BF16, bool HYBRID>
+static cudaError_t bulk_smem_attr() {
+    static int done = 0;   // benign race: the attribute call is idempotent
+    if (done) return cudaSuccess;
+    const int most = 128 + kStages * kChunk * (kBulkMaxRowBytes + 12);
+    cudaError_t e = cudaFuncSetAttribute(reduce_adamw_bulk_kernel<GT, NMAX, BF16, HYBRID>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e == cudaSuccess) done = 1;
+    return e;
+}
+
 template <typename GT, int NMAX, bool BF16>
 static cudaError_t launch_ra_t(const Tile* tiles, int64_t ntiles, const void* const* grads,
                                const ReduceArgs& a, float* gshard, float* p, float* m, float* v,
-                               uint16_t* shadow, const StepSource& c, cudaStream_t st) {
+                               uint16_t* shadow, const StepSource& c, int32_t* kstatus, cudaStream_t st) {
     GradPtrs<NMAX> gp;
     const int W = a.F * a.groups;
     for (int r = 0; r < NMAX; ++r) gp.p[r] = r < W ? grads[r] : nullptr;
+    if (W * static_cast<int>(sizeof(GT)) <= kBulkMaxRowBytes) {
+        const size_t smem = 128 + static_cast<size_t>(kStages) * kChunk * (W * sizeof(GT) + 12);
+        if (a.groups > 1) {
+            cudaError_t e = bulk_smem_attr<GT, NMAX, BF16, true>();
+            if (e != cudaSuccess) return e;
+            return launch_pdl_smem(reduce_adamw_bulk_kernel<GT, NMAX, BF16, true>, grid_for(ntiles), kBlock,
+                                   smem, st, tiles, ntiles, gp, a, gshard, p, m, v, shadow, c, kstatus);
+        }
+        cudaError_t e = bulk_smem_attr<GT, NMAX, BF16, false>();
+        if (e != cudaSuccess) return e;
+        return launch_pdl_smem(reduce_adamw_bulk_kernel<GT, NMAX, BF16, false>, grid_for(ntiles), kBlock,
+                               smem, st, tiles, ntiles, gp, a, gshard, p, m, v, shadow, c, kstatus);
+    }
     if (a.groups > 1)
         return launch_pdl(reduce_adamw_kernel<GT, NMAX, BF16, true>, grid_for(ntiles), kBlock, st, tiles,
                           ntiles, gp, a, gshard, p, m, v, shadow, c);
@@ -841,22 +1176,27 @@ static cudaError_t launch_ra_t(const Tile* tiles, int64_t ntiles, const void* co
 template <typename GT>
 static cudaError_t launch_ra_dt(const Tile* tiles, int64_t ntiles, const void* const* grads,
                                 const ReduceArgs& a, float* gshard, float* p, float* m, float* v,
-                                uint16_t* shadow, const StepSource& c, cudaStream_t st) {
+                                uint16_t* shadow, const StepSource& c, int32_t* ks, cudaStream_t st) {
     const bool small = a.F * a.groups <= 64;
     if (a.bf16_reduce)
-        return small ? launch_ra_t<GT, 64, true>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st)
-                     : launch_ra_t<GT, kMaxRanks, true>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st);
-    return small ? launch_ra_t<GT, 64, false>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st)
-                 : launch_ra_t<GT, kMaxRanks, false>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st);
+        return small ? launch_ra_t<GT, 64, true>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, ks, st)
+                     : launch_ra_t<GT, kMaxRanks, true>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, ks, st);
+    return small ? launch_ra_t<GT, 64, false>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, ks, st)
+                 : launch_ra_t<GT, kMaxRanks, false>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, ks, st);
 }
 
 cudaError_t launch_reduce_adamw(const Tile* tiles, int64_t ntiles, const void* const* grads,
                                 int grad_dtype, const ReduceArgs& a, float* gshard, float* p, float* m,
-                                float* v, uint16_t* shadow, const StepSource& c, cudaStream_t st) {
+                                float* v, uint16_t* shadow, const StepSource& c, int32_t* kstatus,
+                                cudaStream_t st) {
     if (ntiles == 0) return cudaSuccess;
     if (grad_dtype == FSDP_DTYPE_BF16)
-        return launch_ra_dt<uint16_t>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st);
-    return launch_ra_dt<float>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, st);
+        return launch_ra_dt<uint16_t>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, kstatus, st);
+    return launch_ra_dt<float>(tiles, ntiles, grads, a, gshard, p, m, v, shadow, c, kstatus, st);
+}
+
+cudaError_t launch_wait_selftest(int32_t* status, unsigned long long limit_ns, cudaStream_t st) {
+    return launch_pdl(wait_selftest_kernel, 1, 32, st, status, limit_ns);
 }
 
 cudaError_t launch_adamw(int64_t n8, float* p, const float* g, float* m, float* v,

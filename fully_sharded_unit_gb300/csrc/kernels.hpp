@@ -67,9 +67,16 @@ cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t beg
 
 // Fused reduce-scatter (no unscale / accumulation / flag) and AdamW over the
 // unit's segments; a.F * a.groups gradient pointers.
+// kstatus: the unit's device status word (FSDP_KSTATUS_* bits raised by
+// kernels whose bounded waits run out).
 cudaError_t launch_reduce_adamw(const Tile* tiles, int64_t ntiles, const void* const* grads,
                                 int grad_dtype, const ReduceArgs& a, float* gshard, float* p, float* m,
-                                float* v, uint16_t* shadow, const StepSource& c, cudaStream_t st);
+                                float* v, uint16_t* shadow, const StepSource& c, int32_t* kstatus,
+                                cudaStream_t st);
+
+// One CTA waiting up to limit_ns on a barrier nothing completes; raises
+// FSDP_KSTATUS_WAIT_TIMEOUT in *status.
+cudaError_t launch_wait_selftest(int32_t* status, unsigned long long limit_ns, cudaStream_t st);
 
 // n8: number of 8-element groups in the slab (slab length / 8).
 cudaError_t launch_adamw(int64_t n8, float* p, const float* g, float* m, float* v,

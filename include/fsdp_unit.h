@@ -97,6 +97,10 @@ extern "C" {
 #define FSDP_KERNEL_REDUCE_ADAMW   4   /* fused reduce-scatter + AdamW (fsdp_step) */
 #define FSDP_KERNEL_COUNT          5
 
+/* bits of a unit's kernel status word (fsdp_kernel_status) */
+#define FSDP_KSTATUS_WAIT_TIMEOUT  1   /* a kernel gave up waiting for its own copies into
+                                          shared memory; its outputs are incomplete      */
+
 /* ---- plain structs ------------------------------------------------------ */
 typedef struct fsdp_unit fsdp_unit;   /* opaque; one FlatParamHandle ([FSDP] section 4.2) */
 
@@ -270,7 +274,10 @@ FSDP_API int fsdp_adamw_step(fsdp_unit* unit, const fsdp_adamw_hp* hp, void* str
  * out_bf16_dev (forward), gather again when reshard_after_forward is set
  * (backward), reduce-scatter `grads_dev`, AdamW.  Same arguments and rules as
  * the individual calls; all four are checked before any is enqueued.  With
- * fuse_reduce_adamw the last two run as one kernel with the same results. */
+ * fuse_reduce_adamw the last two run as one kernel with the same results;
+ * when W x gradient bytes <= 16 (bf16 gradients with W <= 8, fp32 with
+ * W <= 4) that kernel stages its inputs in shared memory with bounded waits
+ * (see fsdp_kernel_status). */
 FSDP_API int fsdp_step(fsdp_unit* unit, const void* const* grads_dev, uint16_t* out_bf16_dev,
               const fsdp_adamw_hp* hp, void* stream);
 
@@ -350,6 +357,23 @@ FSDP_API int fsdp_unit_segments(const fsdp_unit* unit, fsdp_segment* segs, int64
 FSDP_API int fsdp_memory_report(const fsdp_unit* unit, int rank, int64_t* param_bytes,
                        int64_t* grad_bytes, int64_t* adam_bytes, int64_t* shadow_bytes,
                        int64_t* pad_bytes);
+
+/* ---- kernel status ---------------------------------------------------------- */
+
+/* Kernels that wait on their own asynchronous copies (the shared-memory
+ * staged fused reduce-scatter + AdamW of fsdp_step) bound every wait; a wait
+ * that runs out raises a FSDP_KSTATUS_* bit in the unit's device status word,
+ * and the kernel returns with its outputs incomplete instead of hanging.
+ * fsdp_kernel_status synchronises `stream`, stores the word in *flags
+ * (0: nothing raised) and clears it.  The word starts at 0 at creation. */
+FSDP_API int fsdp_kernel_status(fsdp_unit* unit, int32_t* flags, void* stream);
+
+/* Self-test of the bounded wait on the current device: one CTA waits on an
+ * mbarrier that nothing completes, gives up after `limit_seconds` (1e-3 ..
+ * 10), and reports through a status word like the staged kernel does.
+ * Synchronous on `stream`; *timed_out is 1 when the wait ran out and the
+ * status came back (the expected outcome), and the context stays usable. */
+FSDP_API int fsdp_selftest_bounded_wait(double limit_seconds, int32_t* timed_out, void* stream);
 
 /* ---- profiling ------------------------------------------------------------- */
 

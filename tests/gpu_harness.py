@@ -138,6 +138,7 @@ def run_full(wl: workloads.Workload, unit: int = 0, use_step: bool = False, step
             # the shadow is the cast of the GPU's own master (checked bitwise against that)
             assert_bits_equal(u16(u.get_state("shadow", k)), O.bf16_rne(u.get_state("param", k).cpu().numpy()),
                               f"shadow rank {k}")
+        assert u.kernel_status() == 0, "a kernel raised its status word"
     finally:
         u.close()
     return cmp
@@ -217,6 +218,7 @@ def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None
         final = {w: np.concatenate([u.read_global(w, a, b - a).cpu().numpy() for a, b in windows])
                  for w in ("param", "exp_avg", "exp_avg_sq")}
         shadow = np.concatenate([u16(u.read_global("shadow", a, b - a)) for a, b in windows])
+        assert u.kernel_status() == 0, "a kernel raised its status word"
         del gdev, out
     finally:
         u.close()

@@ -1,4 +1,5 @@
 """The C-ABI library loads (no GPU needed) and exports every declared entry point."""
+import ctypes
 import os
 import re
 import subprocess
@@ -54,3 +55,16 @@ def test_oracle_is_not_imported_by_the_package():
             if f.endswith((".py", ".cu", ".cpp", ".hpp", ".h")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert "from oracle" not in src and "import oracle" not in src, f
+
+
+def test_status_and_selftest_reject_bad_arguments_without_a_device():
+    """Argument checks come before any CUDA call, so they hold on a host
+    without a GPU."""
+    library()
+    from fully_sharded_unit_gb300 import binding as B
+    for limit in (0.0, 1e-4, 20.0, float("nan")):
+        with pytest.raises(B.FsdpError) as e:
+            B.fsdp_selftest_bounded_wait(limit, stream=0)
+        assert e.value.code == B.FSDP_E_INVALID_ARG
+    f = ctypes.c_int32()
+    assert B.lib().fsdp_kernel_status(None, ctypes.byref(f), None) == B.FSDP_E_INVALID_ARG

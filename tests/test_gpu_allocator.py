@@ -12,8 +12,9 @@ import gpu_harness as H
 
 pytestmark = pytest.mark.gpu
 
-# master, gradient shard, m, v, shadow, the two tile tables, the parameter table
-BLOCKS_PER_UNIT = 8
+# master, gradient shard, m, v, shadow, the two tile tables, the parameter
+# table, the kernel status word
+BLOCKS_PER_UNIT = 9
 
 
 @pytest.fixture(scope="module", autouse=True)

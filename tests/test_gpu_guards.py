@@ -37,6 +37,7 @@ def _pads_are_zero(u):
     ("ragged_mini_flat_n3", {"layout": "flat_padded", "gather_source": "shadow"}),
     ("ragged_mini_dim0_n7", {"replicas": 2, "reduce_dtype": "f32"}),
     ("ragged_mini_flat_n8", {"reduce_dtype": "bf16", "fuse_reduce_adamw": True}),
+    ("ragged_mini_dim0_n3", {"fuse_reduce_adamw": True}),           # fp32, W = 3: shared-memory staged
 ])
 def test_pads_stay_zero_and_output_canary_holds(name, kw):
     wl = workloads.get(name).with_(**kw)
@@ -61,5 +62,25 @@ def test_pads_stay_zero_and_output_canary_holds(name, kw):
         torch.cuda.synchronize()
         assert torch.all(out[P:] == CANARY), "gathered output overran its P elements"
         _pads_are_zero(u)
+    finally:
+        u.close()
+
+
+def test_bounded_wait_runs_out_and_reports():
+    """A wait that nothing completes gives up after its limit, the status
+    comes back to the host, and the context stays usable."""
+    import time
+    t0 = time.perf_counter()
+    assert B.fsdp_selftest_bounded_wait(0.05)
+    assert time.perf_counter() - t0 >= 0.05
+    wl = workloads.get("gpt_mini_flat_bf16").with_(fuse_reduce_adamw=True)
+    u = B.Unit(wl.shapes(0), "flat", wl.N, "bf16", fuse_reduce_adamw=True)
+    try:
+        u.load([p.cuda() for p in workloads.param_tensors(wl, 0)])
+        grads = [workloads.grad_tensor(wl, 0, 0, r).cuda() for r in range(wl.N)]
+        out = torch.empty(wl.unit_numel(0), dtype=torch.int16, device="cuda")
+        u.step(grads, out, workloads.hyper(wl))
+        assert u.kernel_status() == 0
+        assert torch.isfinite(u.read_global("param")).all()
     finally:
         u.close()

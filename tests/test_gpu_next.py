@@ -194,6 +194,49 @@ def test_fused_reduce_adamw_step(name, kw):
     assert cmp.total_diff == 0
 
 
+def _staged_eligible(wl):
+    return wl.world * (2 if wl.grad_dtype == "bf16" else 4) <= 16
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("ragged_mini_flat_n3", {}), ("ragged_mini_dim0_n2", {}), ("ragged_mini_flat_n1", {}),
+    ("gpt_mini_flat_bf16", {"N": 4, "replicas": 2}),
+    ("gpt_mini_dim0", {"grad_dtype": "bf16"}),
+    ("ragged_mini_flat_n8", {"grad_dtype": "bf16", "layout": "flat_padded", "gather_source": "shadow"}),
+    ("ragged_mini_dim0_n7", {"grad_dtype": "bf16", "reduce_dtype": "bf16"}),
+    ("ragged_mini_flat_n2", {"replicas": 2}),
+])
+def test_fused_staged_kernel(name, kw):
+    """Units with W x gradient bytes <= 16 take the fused kernel that stages
+    its inputs in shared memory with bulk asynchronous copies: bit-identical
+    to the oracle, status word clear."""
+    wl = workloads.get(name).with_(fuse_reduce_adamw=True, **kw)
+    assert _staged_eligible(wl)
+    cmp = H.run_full(wl, use_step=True)
+    assert cmp.total_diff == 0
+
+
+def _custom(shapes, N, layout, grad_dtype="bf16", steps=3):
+    init = ("uniform", -0.5, 0.5)
+    units = (tuple(workloads.Param(f"p{i}", tuple(s), init) for i, s in enumerate(shapes)),)
+    return workloads.Workload(name="custom", description="custom", units=units, N=N, layout=layout,
+                              grad_dtype=grad_dtype, steps=steps, grad_std=1e-2, fuse_reduce_adamw=True)
+
+
+@pytest.mark.parametrize("layout", ["flat", "dim0"])
+@pytest.mark.parametrize("shapes,N", [
+    ([(1,)], 1), ([(3, 4), (3,)], 8), ([(2, 3), ()], 3), ([(0, 7), (9, 2), (0,)], 4), ([(8193,)], 3),
+    ([(16384 + 5, 3)], 7), ([(2049,), (15,), (17,)], 2), ([(40, 50)], 8), ([(4096 + 16,)], 1),
+])
+def test_fused_staged_edge_shapes(shapes, N, layout):
+    """Tiles with no aligned body, bodies shorter than one chunk, chunks that
+    end mid-tile, empty ranks, one element."""
+    wl = _custom(shapes, N, layout)
+    assert _staged_eligible(wl)
+    H.run_full(wl, use_step=True)
+    H.run_full(wl.with_(grad_dtype="f32", N=min(N, 4)), use_step=True)
+
+
 def test_fused_step_profiles_one_kernel():
     wl = workloads.get("ragged_mini_flat_n8")
     u = B.Unit(wl.shapes(0), "flat", 8, fuse_reduce_adamw=True)
