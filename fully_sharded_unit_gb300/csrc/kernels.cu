@@ -1,12 +1,14 @@
 // Per-unit FSDP kernels for sm_103a: shard-in, gather+cast (from the fp32
 // master or the bf16 shadow), reduce-scatter, AdamW, the fused reduce-scatter
-// + AdamW, a range cast and the device step counter.  All are HBM-bandwidth
-// bound streaming passes; none is a contraction, so no tensor cores are
-// involved.
+// + AdamW (staged in shared memory by bulk asynchronous copies, or in
+// registers for wide units), a range cast, the device step counter and a
+// bounded-wait self-test.  All are HBM-bandwidth bound streaming passes; none
+// is a contraction, so no tensor cores are involved.
 //
 // Memory access: an 8-element group is one 256-bit fp32 access
-// (ld/st .v8.f32) or one 128-bit bf16 access (.v4.b32); the bf16-gradient
-// reduce-scatter reads 16-element groups, one 256-bit access per rank.
+// (ld/st .v8.f32) or one 128-bit bf16 access (.v4.b32); the plain
+// bf16-gradient reduce-scatter reads 16-element groups, one 256-bit access
+// per rank; the staged fused kernel moves whole chunk rows with cp.async.bulk.
 // Segment-driven kernels walk a tile table (see plan.hpp): a tile never spans
 // two segments, and because arena slots are congruent to global indices
 // modulo 32 elements, a group that is aligned in the unsharded buffer is
@@ -16,7 +18,8 @@
 // Launch: every kernel is launched with programmatic stream serialization
 // and starts with griddepcontrol.wait (pdl_enter), so the next kernel's CTAs
 // are scheduled during the previous kernel's last wave while the stream order
-// of every memory access stays the same.
+// of every memory access stays the same (the staged fused kernel waits but
+// does not release its successor early).
 //
 // Numerics: every floating-point operation is an explicitly rounded
 // intrinsic (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so nothing is
