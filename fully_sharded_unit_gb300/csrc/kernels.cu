@@ -736,22 +736,31 @@ __global__ void __launch_bounds__(kBlock, sizeof(GT) == 2 ? 3 : 2) reduce_adamw_
 // ---------------------------------------------------------------- fused reduce-scatter + AdamW, bulk-copy staged
 
 // The fused reduce-scatter + AdamW with its inputs staged in shared memory.
-// A CTA takes one tile and streams it in chunks of kChunk elements through a
+// A CTA takes one tile and streams it in chunks of CH elements through a
 // ring of kStages stages.  A stage holds the chunk's W gradient rows and its
 // p, m, v; one thread brings them in with bulk asynchronous copies
 // (cp.async.bulk, the tensor-memory accelerator's untiled form) counted by the
 // stage's mbarrier, and all threads fold, update and store from shared
 // memory.  The loads in flight live in shared memory instead of registers:
-// 60 registers and no spills against 80 with spills for the register-staged
-// kernel, 7.12 TB/s against 6.74 TB/s on the minGPT unit (bf16 gradients,
-// W = 8).  Measured over chunk x stages: 2048 x 2 (115 KB, 2 CTAs per SM) and
-// 1024 x 3 (86 KB, 2 per SM) within 0.4 %; 512-element chunks (1 KB copies)
-// and 2048 x 3 (1 CTA per SM) 10-35 % slower; one CTA per tile beats 2 or 4
-// tiles per CTA and a persistent grid.  Used when W x gradient bytes <= 16
-// (stage <= 56 KB); wider units take reduce_adamw_kernel.
-constexpr int kChunk = 2048;
+// about 60 registers and no spills against 80 with spills for the
+// register-staged kernel; on the minGPT unit (bf16 gradients, W = 8) 7.12 TB/s
+// against 6.74, and 7.24 against 6.46 TB/s with two replication groups
+// (W = 16).  Measured over chunk x stages at W = 8: 2048 x 2 (115 KB, 2 CTAs
+// per SM) and 1024 x 3 (86 KB, 2 per SM) within 0.4 %; 512-element chunks
+// (1 KB copies) and 2048 x 3 (1 CTA per SM) 10-35 % slower; one CTA per tile
+// beats 2 or 4 tiles per CTA and a persistent grid.  So two stages of at most
+// 56 KB, the chunk the largest of 2048, 1024, 512 elements that fits: up to
+// W x gradient bytes = 100 (bf16 gradients with W <= 50, fp32 with W <= 25);
+// wider units take reduce_adamw_kernel.
 constexpr int kStages = 2;
-constexpr int kBulkMaxRowBytes = 16;   // W * sizeof(GT) limit for the staged kernel
+// A stage holds at most this many bytes (2 CTAs of 2 stages fit an SM); the
+// chunk is the largest of 2048, 1024 and 512 elements that fits.
+constexpr int kStageMaxBytes = 57344;
+__host__ __device__ constexpr int chunk_for(int row_bytes) {   // row_bytes = W * sizeof(GT)
+    return 2048 * (row_bytes + 12) <= kStageMaxBytes ? 2048
+         : 1024 * (row_bytes + 12) <= kStageMaxBytes ? 1024
+         : 512 * (row_bytes + 12) <= kStageMaxBytes ? 512 : 0;
+}
 // A wait on a stage gives up after this long: the kernel then raises bit
 // FSDP_KSTATUS_WAIT_TIMEOUT of the unit's status word, waits (again bounded)
 // for its own copies in flight and returns.
@@ -804,10 +813,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
 }
 
-// Layout of one stage: W gradient rows of kChunk GT, then p, m, v (fp32).
-template <typename GT>
+// Layout of one stage: W gradient rows of CH GT, then p, m, v (fp32).
+template <typename GT, int CH>
 __device__ __forceinline__ size_t stage_bytes(int W) {
-    return static_cast<size_t>(kChunk) * (W * sizeof(GT) + 12);
+    return static_cast<size_t>(CH) * (W * sizeof(GT) + 12);
 }
 
 // The aligned body of a tile: [ga, gb), multiples of 16 elements.
@@ -843,7 +852,7 @@ __device__ __forceinline__ Body tile_body(const Tile& tl) {
 // Four consecutive reduced gradients from a stage, same operation order as
 // reduce8 (fp32 fold within each group, then across groups, then / W; or
 // the bf16 fold).
-template <typename GT, bool BF16>
+template <typename GT, bool BF16, int CH>
 __device__ __forceinline__ void reduce4_smem(const unsigned char* rows, int F, int groups, float fW, int e,
                                              float out[4]) {
     if constexpr (BF16) {
@@ -851,11 +860,11 @@ __device__ __forceinline__ void reduce4_smem(const unsigned char* rows, int F, i
         for (int r = 0; r < F; ++r) {
             uint32_t w[2];
             if constexpr (sizeof(GT) == 2) {
-                const uint2 q = *reinterpret_cast<const uint2*>(rows + (static_cast<size_t>(r) * kChunk + e) * 2);
+                const uint2 q = *reinterpret_cast<const uint2*>(rows + (static_cast<size_t>(r) * CH + e) * 2);
                 w[0] = q.x;
                 w[1] = q.y;
             } else {
-                const float4 q = *reinterpret_cast<const float4*>(rows + (static_cast<size_t>(r) * kChunk + e) * 4);
+                const float4 q = *reinterpret_cast<const float4*>(rows + (static_cast<size_t>(r) * CH + e) * 4);
                 w[0] = pack_bf16x2(q.x, q.y);
                 w[1] = pack_bf16x2(q.z, q.w);
             }
@@ -874,11 +883,11 @@ __device__ __forceinline__ void reduce4_smem(const unsigned char* rows, int F, i
                 const int row = grp * F + r;
                 float x[4];
                 if constexpr (sizeof(GT) == 2) {
-                    const uint2 q = *reinterpret_cast<const uint2*>(rows + (static_cast<size_t>(row) * kChunk + e) * 2);
+                    const uint2 q = *reinterpret_cast<const uint2*>(rows + (static_cast<size_t>(row) * CH + e) * 2);
                     widen2(q.x, x[0], x[1]);
                     widen2(q.y, x[2], x[3]);
                 } else {
-                    const float4 q = *reinterpret_cast<const float4*>(rows + (static_cast<size_t>(row) * kChunk + e) * 4);
+                    const float4 q = *reinterpret_cast<const float4*>(rows + (static_cast<size_t>(row) * CH + e) * 4);
                     x[0] = q.x;
                     x[1] = q.y;
                     x[2] = q.z;
@@ -895,7 +904,7 @@ __device__ __forceinline__ void reduce4_smem(const unsigned char* rows, int F, i
     }
 }
 
-template <typename GT, int NMAX, bool BF16, bool HYBRID>
+template <typename GT, int NMAX, bool BF16, bool HYBRID, int CH>
 __global__ void __launch_bounds__(kBlock) reduce_adamw_bulk_kernel(const Tile* __restrict__ tiles,
                                                                    int64_t ntiles, GradPtrs<NMAX> gp,
                                                                    ReduceArgs a, float* __restrict__ gshard,
@@ -917,7 +926,7 @@ __global__ void __launch_bounds__(kBlock) reduce_adamw_bulk_kernel(const Tile* _
     const int groups = HYBRID ? a.groups : 1;
     const int W = a.F * groups;
     const float fW = static_cast<float>(W);
-    const size_t sbytes = stage_bytes<GT>(W);
+    const size_t sbytes = stage_bytes<GT, CH>(W);
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -936,25 +945,25 @@ __global__ void __launch_bounds__(kBlock) reduce_adamw_bulk_kernel(const Tile* _
                 pb = tile_body(tiles[pt]);
                 pb_valid = true;
             }
-            const int64_t nch = (pb.n + kChunk - 1) / kChunk;
+            const int64_t nch = (pb.n + CH - 1) / CH;
             if (pc >= nch) {
                 pt += gridDim.x;
                 pc = 0;
                 pb_valid = false;
                 continue;
             }
-            const int64_t off = pc * kChunk;
-            const uint32_t n = static_cast<uint32_t>(pb.n - off < kChunk ? pb.n - off : kChunk);
+            const int64_t off = pc * CH;
+            const uint32_t n = static_cast<uint32_t>(pb.n - off < CH ? pb.n - off : CH);
             const int s = static_cast<int>(issued % kStages);
             unsigned char* st = ring + s * sbytes;
             mbar_expect_tx(&full[s], n * static_cast<uint32_t>(W * sizeof(GT) + 12));
             for (int r = 0; r < W; ++r)
-                bulk_g2s(st + static_cast<size_t>(r) * kChunk * sizeof(GT),
+                bulk_g2s(st + static_cast<size_t>(r) * CH * sizeof(GT),
                          static_cast<const GT*>(gp.p[r]) + pb.ga + off, n * sizeof(GT), &full[s]);
-            unsigned char* pmv = st + static_cast<size_t>(W) * kChunk * sizeof(GT);
+            unsigned char* pmv = st + static_cast<size_t>(W) * CH * sizeof(GT);
             bulk_g2s(pmv, p + pb.sa + off, n * 4, &full[s]);
-            bulk_g2s(pmv + kChunk * 4, m + pb.sa + off, n * 4, &full[s]);
-            bulk_g2s(pmv + 2 * kChunk * 4, v + pb.sa + off, n * 4, &full[s]);
+            bulk_g2s(pmv + CH * 4, m + pb.sa + off, n * 4, &full[s]);
+            bulk_g2s(pmv + 2 * CH * 4, v + pb.sa + off, n * 4, &full[s]);
             ++issued;
             ++pc;
         }
@@ -979,22 +988,22 @@ __global__ void __launch_bounds__(kBlock) reduce_adamw_bulk_kernel(const Tile* _
             v[s] = vv;
             shadow[s] = to_bf16(pp);
         }
-        const int64_t nch = (b.n + kChunk - 1) / kChunk;
+        const int64_t nch = (b.n + CH - 1) / CH;
         for (int64_t ch = 0; ch < nch; ++ch) {
             if (tid == 0) top_up();
             const int s = static_cast<int>(consumed % kStages);
             const uint32_t parity = (consumed / kStages) & 1u;
             const bool got = mbar_wait(&full[s], parity);
-            const int64_t off = ch * kChunk;
-            const int64_t n = b.n - off < kChunk ? b.n - off : kChunk;
+            const int64_t off = ch * CH;
+            const int64_t n = b.n - off < CH ? b.n - off : CH;
             for (int e = tid * 4; got && e < n; e += 4 * kBlock) {
                 const unsigned char* st = ring + s * sbytes;
                 float G[4];
-                reduce4_smem<GT, BF16>(st, a.F, groups, fW, e, G);
-                const float* pmv = reinterpret_cast<const float*>(st + static_cast<size_t>(W) * kChunk * sizeof(GT));
+                reduce4_smem<GT, BF16, CH>(st, a.F, groups, fW, e, G);
+                const float* pmv = reinterpret_cast<const float*>(st + static_cast<size_t>(W) * CH * sizeof(GT));
                 float4 P = *reinterpret_cast<const float4*>(pmv + e);
-                float4 M = *reinterpret_cast<const float4*>(pmv + kChunk + e);
-                float4 V = *reinterpret_cast<const float4*>(pmv + 2 * kChunk + e);
+                float4 M = *reinterpret_cast<const float4*>(pmv + CH + e);
+                float4 V = *reinterpret_cast<const float4*>(pmv + 2 * CH + e);
                 adamw_elem(P.x, G[0], M.x, V.x, c);
                 adamw_elem(P.y, G[1], M.y, V.y, c);
                 adamw_elem(P.z, G[2], M.z, V.z, c);
@@ -1138,15 +1147,38 @@ cudaError_t launch_reduce_scatter(const Tile* tiles, int64_t ntiles, const void*
 
 // The staged kernel needs more than the default 48 KB of dynamic shared
 // memory: raise the kernel's limit once per instantiation.
-template <typename GT, int NMAX, bool BF16, bool HYBRID>
+template <typename GT, int NMAX, bool BF16, bool HYBRID, int CH>
 static cudaError_t bulk_smem_attr() {
     static int done = 0;   // benign race: the attribute call is idempotent
     if (done) return cudaSuccess;
-    const int most = 128 + kStages * kChunk * (kBulkMaxRowBytes + 12);
-    cudaError_t e = cudaFuncSetAttribute(reduce_adamw_bulk_kernel<GT, NMAX, BF16, HYBRID>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    cudaError_t e = cudaFuncSetAttribute(reduce_adamw_bulk_kernel<GT, NMAX, BF16, HYBRID, CH>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         128 + kStages * kStageMaxBytes);
     if (e == cudaSuccess) done = 1;
     return e;
+}
+
+template <typename GT, int NMAX, bool BF16, bool HYBRID, int CH>
+static cudaError_t launch_bulk(const Tile* tiles, int64_t ntiles, const GradPtrs<NMAX>& gp, const ReduceArgs& a,
+                               float* gshard, float* p, float* m, float* v, uint16_t* shadow,
+                               const StepSource& c, int32_t* kstatus, cudaStream_t st) {
+    const int W = a.F * a.groups;
+    const size_t smem = 128 + static_cast<size_t>(kStages) * CH * (W * sizeof(GT) + 12);
+    cudaError_t e = bulk_smem_attr<GT, NMAX, BF16, HYBRID, CH>();
+    if (e != cudaSuccess) return e;
+    return launch_pdl_smem(reduce_adamw_bulk_kernel<GT, NMAX, BF16, HYBRID, CH>, grid_for(ntiles), kBlock, smem,
+                           st, tiles, ntiles, gp, a, gshard, p, m, v, shadow, c, kstatus);
+}
+
+template <typename GT, int NMAX, bool BF16, bool HYBRID>
+static cudaError_t launch_bulk_ch(int ch, const Tile* tiles, int64_t ntiles, const GradPtrs<NMAX>& gp,
+                                  const ReduceArgs& a, float* gshard, float* p, float* m, float* v,
+                                  uint16_t* shadow, const StepSource& c, int32_t* kstatus, cudaStream_t st) {
+    if (ch == 2048)
+        return launch_bulk<GT, NMAX, BF16, HYBRID, 2048>(tiles, ntiles, gp, a, gshard, p, m, v, shadow, c, kstatus, st);
+    if (ch == 1024)
+        return launch_bulk<GT, NMAX, BF16, HYBRID, 1024>(tiles, ntiles, gp, a, gshard, p, m, v, shadow, c, kstatus, st);
+    return launch_bulk<GT, NMAX, BF16, HYBRID, 512>(tiles, ntiles, gp, a, gshard, p, m, v, shadow, c, kstatus, st);
 }
 
 template <typename GT, int NMAX, bool BF16>
@@ -1156,18 +1188,15 @@ static cudaError_t launch_ra_t(const Tile* tiles, int64_t ntiles, const void* co
     GradPtrs<NMAX> gp;
     const int W = a.F * a.groups;
     for (int r = 0; r < NMAX; ++r) gp.p[r] = r < W ? grads[r] : nullptr;
-    if (W * static_cast<int>(sizeof(GT)) <= kBulkMaxRowBytes) {
-        const size_t smem = 128 + static_cast<size_t>(kStages) * kChunk * (W * sizeof(GT) + 12);
-        if (a.groups > 1) {
-            cudaError_t e = bulk_smem_attr<GT, NMAX, BF16, true>();
-            if (e != cudaSuccess) return e;
-            return launch_pdl_smem(reduce_adamw_bulk_kernel<GT, NMAX, BF16, true>, grid_for(ntiles), kBlock,
-                                   smem, st, tiles, ntiles, gp, a, gshard, p, m, v, shadow, c, kstatus);
+    if constexpr (NMAX <= 64) {   // wider units never fit a stage
+        const int ch = chunk_for(W * static_cast<int>(sizeof(GT)));
+        if (ch > 0) {
+            if (a.groups > 1)
+                return launch_bulk_ch<GT, NMAX, BF16, true>(ch, tiles, ntiles, gp, a, gshard, p, m, v, shadow, c,
+                                                            kstatus, st);
+            return launch_bulk_ch<GT, NMAX, BF16, false>(ch, tiles, ntiles, gp, a, gshard, p, m, v, shadow, c,
+                                                         kstatus, st);
         }
-        cudaError_t e = bulk_smem_attr<GT, NMAX, BF16, false>();
-        if (e != cudaSuccess) return e;
-        return launch_pdl_smem(reduce_adamw_bulk_kernel<GT, NMAX, BF16, false>, grid_for(ntiles), kBlock,
-                               smem, st, tiles, ntiles, gp, a, gshard, p, m, v, shadow, c, kstatus);
     }
     if (a.groups > 1)
         return launch_pdl(reduce_adamw_kernel<GT, NMAX, BF16, true>, grid_for(ntiles), kBlock, st, tiles,

@@ -275,8 +275,8 @@ FSDP_API int fsdp_adamw_step(fsdp_unit* unit, const fsdp_adamw_hp* hp, void* str
  * (backward), reduce-scatter `grads_dev`, AdamW.  Same arguments and rules as
  * the individual calls; all four are checked before any is enqueued.  With
  * fuse_reduce_adamw the last two run as one kernel with the same results;
- * when W x gradient bytes <= 16 (bf16 gradients with W <= 8, fp32 with
- * W <= 4) that kernel stages its inputs in shared memory with bounded waits
+ * when W x gradient bytes <= 100 (bf16 gradients with W <= 50, fp32 with
+ * W <= 25) that kernel stages its inputs in shared memory with bounded waits
  * (see fsdp_kernel_status). */
 FSDP_API int fsdp_step(fsdp_unit* unit, const void* const* grads_dev, uint16_t* out_bf16_dev,
               const fsdp_adamw_hp* hp, void* stream);

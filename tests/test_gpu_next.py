@@ -195,7 +195,8 @@ def test_fused_reduce_adamw_step(name, kw):
 
 
 def _staged_eligible(wl):
-    return wl.world * (2 if wl.grad_dtype == "bf16" else 4) <= 16
+    """The shared-memory staged fused kernel takes W x gradient bytes <= 100."""
+    return wl.world * (2 if wl.grad_dtype == "bf16" else 4) <= 100
 
 
 @pytest.mark.parametrize("name,kw", [
@@ -205,9 +206,13 @@ def _staged_eligible(wl):
     ("ragged_mini_flat_n8", {"grad_dtype": "bf16", "layout": "flat_padded", "gather_source": "shadow"}),
     ("ragged_mini_dim0_n7", {"grad_dtype": "bf16", "reduce_dtype": "bf16"}),
     ("ragged_mini_flat_n2", {"replicas": 2}),
+    ("ragged_mini_flat_n8", {}),                                  # 1024-element chunks
+    ("gpt_mini_flat_bf16", {"N": 8, "replicas": 2}),              # W = 16, 1024-element chunks
+    ("ragged_mini_dim0_n7", {"replicas": 3}),                     # fp32, W = 21, 512-element chunks
+    ("ragged_mini_flat_n3", {"N": 25}),                           # fp32, W = 25: the widest staged unit
 ])
 def test_fused_staged_kernel(name, kw):
-    """Units with W x gradient bytes <= 16 take the fused kernel that stages
+    """Units with W x gradient bytes <= 100 take the fused kernel that stages
     its inputs in shared memory with bulk asynchronous copies: bit-identical
     to the oracle, status word clear."""
     wl = workloads.get(name).with_(fuse_reduce_adamw=True, **kw)
@@ -234,7 +239,7 @@ def test_fused_staged_edge_shapes(shapes, N, layout):
     wl = _custom(shapes, N, layout)
     assert _staged_eligible(wl)
     H.run_full(wl, use_step=True)
-    H.run_full(wl.with_(grad_dtype="f32", N=min(N, 4)), use_step=True)
+    H.run_full(wl.with_(grad_dtype="f32"), use_step=True)
 
 
 def test_fused_step_profiles_one_kernel():
