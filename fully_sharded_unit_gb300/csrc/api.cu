@@ -308,7 +308,7 @@ int enqueue_reduce_scatter(fsdp_unit* u, const void* const* grads, const fsdp_rs
         }
     }
     return profiled_launch(u, FSDP_KERNEL_REDUCE_SCATTER, st, "reduce-scatter launch", [&] {
-        return fsdp::launch_reduce_scatter(u->tiles, u->ntiles, grads, u->grad_dtype, a, u->grad, st);
+        return fsdp::launch_reduce_scatter(u->tiles, u->ntiles, grads, u->grad_dtype, a, u->grad, u->kstatus, st);
     });
 }
 

@@ -58,8 +58,10 @@ cudaError_t launch_gather_shadow(const Tile* tiles, int64_t ntiles, const uint16
                                  uint16_t* out, cudaStream_t st);
 
 // grads: W = a.F * a.groups pointers (fp32 or bf16 per grad_dtype), each P elements.
+// kstatus: the unit's device status word (FSDP_KSTATUS_* bits).
 cudaError_t launch_reduce_scatter(const Tile* tiles, int64_t ntiles, const void* const* grads,
-                                  int grad_dtype, const ReduceArgs& a, float* gshard, cudaStream_t st);
+                                  int grad_dtype, const ReduceArgs& a, float* gshard, int32_t* kstatus,
+                                  cudaStream_t st);
 
 // shadow[i] = RNE_bf16(master[i]) for i in [begin, begin + n); begin and n
 // multiples of 8.

@@ -361,7 +361,9 @@ FSDP_API int fsdp_memory_report(const fsdp_unit* unit, int rank, int64_t* param_
 /* ---- kernel status ---------------------------------------------------------- */
 
 /* Kernels that wait on their own asynchronous copies (the shared-memory
- * staged fused reduce-scatter + AdamW of fsdp_step) bound every wait; a wait
+ * staged fused reduce-scatter + AdamW of fsdp_step, and the staged
+ * reduce-scatter that serves hybrid sharding, accumulation, unscaling and the
+ * non-finite flag when W x gradient bytes <= 100) bound every wait; a wait
  * that runs out raises a FSDP_KSTATUS_* bit in the unit's device status word,
  * and the kernel returns with its outputs incomplete instead of hanging.
  * fsdp_kernel_status synchronises `stream`, stores the word in *flags
