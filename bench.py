@@ -103,10 +103,24 @@ def kernel_source_sha() -> str:
     return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
+def traffic_key(wl: workloads.Workload, micro_batches: int = 1) -> str:
+    """The workload name plus every option that changes a kernel's bytes per
+    launch (a capture applies only to the configuration it was taken on)."""
+    key = wl.name
+    base = workloads.get(wl.name)
+    for name in ("layout", "replicas", "reduce_dtype", "gather_source", "grad_dtype", "N"):
+        if getattr(wl, name) != getattr(base, name):
+            key += f"+{name}={getattr(wl, name)}"
+    if micro_batches > 1:
+        key += f"+micro_batches={micro_batches}"
+    return key
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary line
-    `kernel workload bytes_per_launch kernels_cu_sha`; None when absent or
-    when the kernel source has changed since the capture."""
+    `kernel workload bytes_per_launch kernels_cu_sha` (workload as
+    traffic_key gives it); None when absent or when the kernel source has
+    changed since the capture."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -377,7 +391,7 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peak()
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": peak_kind,
-                "traffic": recorded_traffic(dom, wl.name),
+                "traffic": recorded_traffic(dom, traffic_key(wl, args.micro_batches)),
                 "per_kernel_ms_per_launch": {k: (v[0] / v[1] if v[1] else None) for k, v in per_kernel.items()},
                 "per_kernel_gbs": {k: (sum(per_step.get(k, lambda c: c[k])(c) for c in cb) /
                                        (v[1] / args.steps) / (v[0] / v[1] * 1e-3) / 1e9 if v[1] else None)
