@@ -27,9 +27,13 @@ def _state(u):
 
 
 @pytest.mark.parametrize("name,kw", [("gpt_mini_flat_bf16", {}), ("gpt_mini_dim0", {"fuse_reduce_adamw": True}),
-                                     ("ragged_mini_flat_n7", {"gather_source": "shadow"})])
+                                     ("ragged_mini_flat_n7", {"gather_source": "shadow"}),
+                                     ("gpt_mini_flat_bf16", {"replicas": 2}),
+                                     ("gpt_mini_flat_bf16", {"replicas": 2, "fuse_reduce_adamw": True})])
 def test_graph_replay_equals_ordinary_steps(name, kw):
-    wl = workloads.get(name)
+    """Also with the shared-memory staged kernels inside the graph (the fused
+    step, and the reduce-scatter of hybrid sharding)."""
+    wl = workloads.get(name).with_(replicas=kw.get("replicas", 1))
     hp = workloads.hyper(wl)
     steps = 4
     ref, gra = _units(wl, **kw), _units(wl, **kw)
