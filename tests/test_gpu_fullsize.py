@@ -63,6 +63,19 @@ def test_unit_past_2_31_elements(name):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("name,kw", [("huge_flat_n3", dict(fuse_reduce_adamw=True)),
+                                     ("huge_dim0_n3", dict(replicas=2)),
+                                     ("huge_flat_n3", dict(replicas=2, fuse_reduce_adamw=True))])
+def test_staged_kernels_past_2_31_elements(name, kw):
+    """The shared-memory staged kernels (fused step; reduce-scatter of hybrid
+    sharding) on a unit past 2^31 elements: 64-bit chunk offsets and copy
+    addresses, windows at every shard boundary and at 2^31."""
+    wl = workloads.get(name).with_(**kw)
+    cmp = H.run_windowed(wl, extra_boundaries=(2 ** 31, 2 ** 31 - 8192))
+    assert cmp.covered > 1_000_000
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("kw", [
     dict(replicas=2),                                   # hybrid: 2 sharding groups of 8, W = 16 gradients
     dict(reduce_dtype="bf16"),                          # reductions in bf16
