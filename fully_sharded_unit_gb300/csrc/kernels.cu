@@ -1183,6 +1183,23 @@ unsigned grid_for(int64_t work) {
 
 // Launch `kernel` on `grid` CTAs of `block` threads with programmatic stream
 // serialization (see pdl_enter).
+// Raise `kernel`'s dynamic shared-memory limit to the staged kernels' most,
+// once per kernel and device (the attribute belongs to the device's context).
+// `done` is the caller's per-kernel array of flags; a benign race at worst
+// repeats the idempotent call.
+constexpr int kMaxDevices = 64;
+
+template <typename... KArgs>
+cudaError_t allow_staged_smem(void (*kernel)(KArgs...), int* done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices && done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 + kStages * kStageMaxBytes);
+    if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev] = 1;
+    return e;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl_smem(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
                             cudaStream_t st, Args... args) {
@@ -1235,14 +1252,9 @@ cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t beg
 template <typename GT, int NMAX, bool BF16, int CH>
 static cudaError_t launch_rs_bulk(const Tile* tiles, int64_t ntiles, const GradPtrs<NMAX>& gp,
                                   const ReduceArgs& a, float* gshard, int32_t* kstatus, cudaStream_t st) {
-    static int done = 0;   // raise the dynamic shared-memory limit once per instantiation
-    if (!done) {
-        cudaError_t e = cudaFuncSetAttribute(reduce_scatter_bulk_kernel<GT, NMAX, BF16, CH>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             128 + kStages * kStageMaxBytes);
-        if (e != cudaSuccess) return e;
-        done = 1;
-    }
+    static int done[kMaxDevices] = {};
+    cudaError_t e = allow_staged_smem(reduce_scatter_bulk_kernel<GT, NMAX, BF16, CH>, done);
+    if (e != cudaSuccess) return e;
     const int W = a.F * a.groups;
     const size_t smem = 128 + static_cast<size_t>(kStages) * CH * (W * sizeof(GT) + (a.accumulate ? 4 : 0));
     return launch_pdl_smem(reduce_scatter_bulk_kernel<GT, NMAX, BF16, CH>, grid_for(ntiles), kBlock, smem, st,
@@ -1296,16 +1308,11 @@ cudaError_t launch_reduce_scatter(const Tile* tiles, int64_t ntiles, const void*
 }
 
 // The staged kernel needs more than the default 48 KB of dynamic shared
-// memory: raise the kernel's limit once per instantiation.
+// memory: raise the kernel's limit once per instantiation and device.
 template <typename GT, int NMAX, bool BF16, bool HYBRID, int CH>
 static cudaError_t bulk_smem_attr() {
-    static int done = 0;   // benign race: the attribute call is idempotent
-    if (done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(reduce_adamw_bulk_kernel<GT, NMAX, BF16, HYBRID, CH>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         128 + kStages * kStageMaxBytes);
-    if (e == cudaSuccess) done = 1;
-    return e;
+    static int done[kMaxDevices] = {};
+    return allow_staged_smem(reduce_adamw_bulk_kernel<GT, NMAX, BF16, HYBRID, CH>, done);
 }
 
 template <typename GT, int NMAX, bool BF16, bool HYBRID, int CH>
