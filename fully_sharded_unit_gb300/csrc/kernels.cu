@@ -1045,7 +1045,7 @@ __global__ void __launch_bounds__(kBlock) reduce_adamw_bulk_kernel(const Tile* _
 // register-staged: staged, it was 1 % slower with bf16 gradients (5.03
 // against 4.98 ms) and 2 % slower with fp32 ones (GPT-2-Large, 0.114 against
 // 0.111 ms).
-template <typename GT, int NMAX, bool BF16, int CH>
+template <typename GT, int NMAX, bool BF16, int CH, int S>
 __global__ void __launch_bounds__(kBlock) reduce_scatter_bulk_kernel(const Tile* __restrict__ tiles,
                                                                      int64_t ntiles, GradPtrs<NMAX> gp,
                                                                      ReduceArgs a, float* __restrict__ gshard,
@@ -1063,7 +1063,7 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_bulk_kernel(const Tile*
     const size_t sbytes = rows_bytes + (acc ? static_cast<size_t>(CH) * 4 : 0);
     const uint32_t elem_bytes = static_cast<uint32_t>(W * sizeof(GT) + (acc ? 4 : 0));
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -1074,7 +1074,7 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_bulk_kernel(const Tile*
     bool pb_valid = false;
     uint32_t issued = 0, consumed = 0;
     auto top_up = [&]() {
-        while (issued - consumed < static_cast<uint32_t>(kStages) && pt < ntiles) {
+        while (issued - consumed < static_cast<uint32_t>(S) && pt < ntiles) {
             if (!pb_valid) {
                 pb = tile_body(tiles[pt]);
                 pb_valid = true;
@@ -1088,7 +1088,7 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_bulk_kernel(const Tile*
             }
             const int64_t off = pc * CH;
             const uint32_t n = static_cast<uint32_t>(pb.n - off < CH ? pb.n - off : CH);
-            const int s = static_cast<int>(issued % kStages);
+            const int s = static_cast<int>(issued % S);
             unsigned char* st = ring + s * sbytes;
             mbar_expect_tx(&full[s], n * elem_bytes);
             for (int r = 0; r < W; ++r)
@@ -1118,8 +1118,8 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_bulk_kernel(const Tile*
         const int64_t nch = (b.n + CH - 1) / CH;
         for (int64_t ch = 0; ch < nch; ++ch) {
             if (tid == 0) top_up();
-            const int s = static_cast<int>(consumed % kStages);
-            const uint32_t parity = (consumed / kStages) & 1u;
+            const int s = static_cast<int>(consumed % S);
+            const uint32_t parity = (consumed / S) & 1u;
             const bool got = mbar_wait(&full[s], parity);
             const int64_t off = ch * CH;
             const int64_t n = b.n - off < CH ? b.n - off : CH;
@@ -1150,7 +1150,7 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_bulk_kernel(const Tile*
     }
     if (!ok && tid == 0) {
         atomicOr(kstatus, FSDP_KSTATUS_WAIT_TIMEOUT);
-        for (uint32_t q = consumed - 1; q < issued; ++q) mbar_wait(&full[q % kStages], (q / kStages) & 1u);
+        for (uint32_t q = consumed - 1; q < issued; ++q) mbar_wait(&full[q % S], (q / S) & 1u);
     }
     if (__syncthreads_or(bad) && tid == 0 && a.found != nullptr) *a.found = 1;
 }
@@ -1249,15 +1249,35 @@ cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t beg
                       shadow + begin, n8);
 }
 
-template <typename GT, int NMAX, bool BF16, int CH>
+// Stages and chunk of the staged reduce-scatter for `bpe` stage bytes per
+// element.  Three CTAs per SM (each at most 75 KB) matter most: two stages of
+// 2048 elements when they fit that budget, else three stages of 1024 when
+// those do, else two stages of at most 56 KB as for the fused kernel.
+// Measured on the minGPT unit (bf16 gradients, W = 8): accumulating (20 bytes
+// per element) 5.88 ms with 3 x 1024 against 6.10 with 2 x 2048 (2 CTAs per
+// SM); the flag or unscale alone (16 bytes) 5.04 ms with 2 x 2048 against
+// 5.08 with 3 x 1024; two replication groups (32 bytes) 9.18 ms with
+// 2 x 1024 against 10.70 with 3 x 1024 (2 CTAs per SM).
+constexpr int kThreeCtaBytes = 76800;
+struct StagePlan {
+    int stages;
+    int chunk;
+};
+constexpr StagePlan rs_plan(int bpe) {
+    return 2 * 2048 * bpe <= kThreeCtaBytes   ? StagePlan{2, 2048}
+           : 3 * 1024 * bpe <= kThreeCtaBytes ? StagePlan{3, 1024}
+                                              : StagePlan{2, chunk_for(bpe)};
+}
+
+template <typename GT, int NMAX, bool BF16, int CH, int S>
 static cudaError_t launch_rs_bulk(const Tile* tiles, int64_t ntiles, const GradPtrs<NMAX>& gp,
                                   const ReduceArgs& a, float* gshard, int32_t* kstatus, cudaStream_t st) {
     static int done[kMaxDevices] = {};
-    cudaError_t e = allow_staged_smem(reduce_scatter_bulk_kernel<GT, NMAX, BF16, CH>, done);
+    cudaError_t e = allow_staged_smem(reduce_scatter_bulk_kernel<GT, NMAX, BF16, CH, S>, done);
     if (e != cudaSuccess) return e;
     const int W = a.F * a.groups;
-    const size_t smem = 128 + static_cast<size_t>(kStages) * CH * (W * sizeof(GT) + (a.accumulate ? 4 : 0));
-    return launch_pdl_smem(reduce_scatter_bulk_kernel<GT, NMAX, BF16, CH>, grid_for(ntiles), kBlock, smem, st,
+    const size_t smem = 128 + static_cast<size_t>(S) * CH * (W * sizeof(GT) + (a.accumulate ? 4 : 0));
+    return launch_pdl_smem(reduce_scatter_bulk_kernel<GT, NMAX, BF16, CH, S>, grid_for(ntiles), kBlock, smem, st,
                            tiles, ntiles, gp, a, gshard, kstatus);
 }
 
@@ -1269,10 +1289,11 @@ static cudaError_t launch_rs_t(const Tile* tiles, int64_t ntiles, const void* co
     for (int r = 0; r < NMAX; ++r) gp.p[r] = r < W ? grads[r] : nullptr;
     if constexpr (NMAX <= 64) {
         if (EXT) {   // the plain form is faster register-staged
-            const int ch = chunk_for(W * static_cast<int>(sizeof(GT)) + (a.accumulate ? 4 : 0));
-            if (ch == 2048) return launch_rs_bulk<GT, NMAX, BF16, 2048>(tiles, ntiles, gp, a, gshard, kstatus, st);
-            if (ch == 1024) return launch_rs_bulk<GT, NMAX, BF16, 1024>(tiles, ntiles, gp, a, gshard, kstatus, st);
-            if (ch == 512) return launch_rs_bulk<GT, NMAX, BF16, 512>(tiles, ntiles, gp, a, gshard, kstatus, st);
+            const StagePlan sp = rs_plan(W * static_cast<int>(sizeof(GT)) + (a.accumulate ? 4 : 0));
+            if (sp.stages == 3) return launch_rs_bulk<GT, NMAX, BF16, 1024, 3>(tiles, ntiles, gp, a, gshard, kstatus, st);
+            if (sp.chunk == 2048) return launch_rs_bulk<GT, NMAX, BF16, 2048, 2>(tiles, ntiles, gp, a, gshard, kstatus, st);
+            if (sp.chunk == 1024) return launch_rs_bulk<GT, NMAX, BF16, 1024, 2>(tiles, ntiles, gp, a, gshard, kstatus, st);
+            if (sp.chunk == 512) return launch_rs_bulk<GT, NMAX, BF16, 512, 2>(tiles, ntiles, gp, a, gshard, kstatus, st);
         }
     }
     return launch_pdl(reduce_scatter_kernel<GT, NMAX, BF16, EXT>, grid_for(ntiles), kBlock, st, tiles, ntiles,
