@@ -182,7 +182,8 @@ FSDP_API int fsdp_plan_layout(int nparams, const int* ndims, const int64_t* dims
 FSDP_API int fsdp_unit_create(int nparams, const int* ndims, const int64_t* dims,
                      const fsdp_unit_config* cfg, fsdp_unit** out);
 
-/* Optional provider of the unit's device memory, for
+/* Optional provider of the unit's device memory (library infrastructure; the
+ * pages have no counterpart), for
  * fsdp_unit_create_with_allocator (so that, for instance, a framework's
  * caching allocator owns and accounts for the rank arenas).  alloc(bytes,
  * ctx) returns a block of device memory on the current device, aligned to at
@@ -289,6 +290,9 @@ FSDP_API int fsdp_step(fsdp_unit* unit, const void* const* grads_dev, uint16_t* 
 FSDP_API int fsdp_unit_set_step_options(fsdp_unit* unit, int gather_source, int fuse_reduce_adamw);
 
 /* ---- state access (tests, checkpoint / resume) --------------------------- */
+/* Library infrastructure: the pages describe the sharded state ([FSDP] 3.2.1,
+ * the FlatParameter owns its shards) but no access calls; these expose it per
+ * rank, in unsharded order, and with the pads, for checkpoints and checks. */
 
 /* Copy rank `rank`'s packed shard of state `which` (pads excluded; fp32, or
  * bf16 for FSDP_STATE_SHADOW) to `dst`, or from `src` into the unit.  dst/src
@@ -312,7 +316,8 @@ FSDP_API int fsdp_read_global(const fsdp_unit* unit, int which, int64_t begin, i
 FSDP_API int fsdp_read_arena(const fsdp_unit* unit, int which, int rank, void* dst, int64_t* arena_len,
                              void* stream);
 
-/* Device-side AdamW step counter, for replaying a captured CUDA graph.
+/* Device-side AdamW step counter, for replaying a captured CUDA graph
+ * (library infrastructure; the pages have no counterpart).
  * Normally the step count t lives on the host and each AdamW launch carries
  * its bias-correction constants, so a captured launch would replay the same
  * step forever.  This call forms, on the host and with the same formulas as
@@ -360,7 +365,8 @@ FSDP_API int fsdp_memory_report(const fsdp_unit* unit, int rank, int64_t* param_
 
 /* ---- kernel status ---------------------------------------------------------- */
 
-/* Kernels that wait on their own asynchronous copies (the shared-memory
+/* Library infrastructure (the pages have no counterpart).
+ * Kernels that wait on their own asynchronous copies (the shared-memory
  * staged fused reduce-scatter + AdamW of fsdp_step, and the staged
  * reduce-scatter that serves hybrid sharding, accumulation, unscaling and the
  * non-finite flag when W x gradient bytes <= 100) bound every wait; a wait
@@ -370,7 +376,8 @@ FSDP_API int fsdp_memory_report(const fsdp_unit* unit, int rank, int64_t* param_
  * (0: nothing raised) and clears it.  The word starts at 0 at creation. */
 FSDP_API int fsdp_kernel_status(fsdp_unit* unit, int32_t* flags, void* stream);
 
-/* Self-test of the bounded wait on the current device: one CTA waits on an
+/* Library infrastructure (the pages have no counterpart).
+ * Self-test of the bounded wait on the current device: one CTA waits on an
  * mbarrier that nothing completes, gives up after `limit_seconds` (1e-3 ..
  * 10), and reports through a status word like the staged kernel does.
  * Synchronous on `stream`; *timed_out is 1 when the wait ran out and the
@@ -378,6 +385,7 @@ FSDP_API int fsdp_kernel_status(fsdp_unit* unit, int32_t* flags, void* stream);
 FSDP_API int fsdp_selftest_bounded_wait(double limit_seconds, int32_t* timed_out, void* stream);
 
 /* ---- profiling ------------------------------------------------------------- */
+/* Library infrastructure (the pages have no counterpart). */
 
 /* While enabled, every kernel the unit launches is bracketed by CUDA events
  * recorded on its launch stream (launches on a stream that is being captured
@@ -390,6 +398,7 @@ FSDP_API int fsdp_profile_read(fsdp_unit* unit, int kernel, double* total_ms, in
 FSDP_API int fsdp_profile_reset(fsdp_unit* unit);
 
 /* ---- host-resident buffers -------------------------------------------------- */
+/* Library infrastructure (the pages have no counterpart). */
 
 /* Device address of pinned (page-locked, mapped) host memory, e.g. from
  * cudaHostAlloc or a pinned torch tensor.  Gradient buffers given to
@@ -399,6 +408,7 @@ FSDP_API int fsdp_profile_reset(fsdp_unit* unit);
 FSDP_API int fsdp_host_device_pointer(const void* host, void** dev);
 
 /* ---- errors -------------------------------------------------------------- */
+/* Library infrastructure (the pages have no counterpart). */
 FSDP_API const char* fsdp_strerror(int code);
 FSDP_API const char* fsdp_last_error(void);    /* calling thread's latest failure reason */
 
