@@ -49,6 +49,8 @@ FSDP_KERNEL_COUNT = 5
 
 FSDP_KSTATUS_WAIT_TIMEOUT = 1
 
+FSDP_NOALLOC_MAX_TILES = 32768
+
 LAYOUTS = {"flat": FSDP_LAYOUT_FLAT, "dim0": FSDP_LAYOUT_DIM0, "flat_padded": FSDP_LAYOUT_FLAT_PADDED}
 GRAD_DTYPES = {"f32": FSDP_DTYPE_F32, "bf16": FSDP_DTYPE_BF16}
 GATHER_SOURCES = {"master": FSDP_GATHER_FROM_MASTER, "shadow": FSDP_GATHER_FROM_SHADOW}
@@ -115,6 +117,7 @@ _SIGNATURES = {
     "fsdp_zero_grad": (_I, [_P, _P]),
     "fsdp_adamw_step": (_I, [_P, ctypes.POINTER(AdamWHp), _P]),
     "fsdp_step": (_I, [_P, ctypes.POINTER(_P), _P, ctypes.POINTER(AdamWHp), _P]),
+    "fsdp_reduce_scatter_flat_noalloc": (_I, [ctypes.POINTER(_P), _I, _I, _I64, _P, _P]),
     "fsdp_get_state": (_I, [_P, _I, _I, _P, _P]),
     "fsdp_set_state": (_I, [_P, _I, _I, _P, _P]),
     "fsdp_read_global": (_I, [_P, _I, _I64, _I64, _P, _P]),
@@ -341,6 +344,24 @@ def fsdp_step(h, grads, out: torch.Tensor, hp, stream=None) -> None:
     hp = _hp(hp)
     _check(lib().fsdp_step(h, _ptrs(grads), out.data_ptr(), ctypes.byref(hp), _stream(stream)),
            "fsdp_step")
+
+
+def fsdp_reduce_scatter_flat_noalloc(grads, out: torch.Tensor, numel: int | None = None, stream=None) -> None:
+    """The FLAT reduce-scatter that allocates nothing: ``grads`` are the N
+    ranks' full gradients (fp32 or bf16 CUDA tensors of one dtype), ``out`` an
+    fp32 CUDA tensor that receives every rank's shard back to back (rank k's at
+    [floor(k*numel/N), floor((k+1)*numel/N))).  ``numel`` defaults to
+    out.numel()."""
+    numel = out.numel() if numel is None else int(numel)
+    assert len(grads) >= 1 and len({g.dtype for g in grads}) == 1
+    dt = grads[0].dtype
+    assert dt in (torch.float32, torch.bfloat16), f"gradient dtype {dt}"
+    for g in grads:
+        assert g.is_cuda and g.is_contiguous() and g.numel() >= numel
+    assert out.is_cuda and out.is_contiguous() and out.dtype == torch.float32 and out.numel() >= numel
+    gd = FSDP_DTYPE_F32 if dt == torch.float32 else FSDP_DTYPE_BF16
+    _check(lib().fsdp_reduce_scatter_flat_noalloc(_ptrs(grads), len(grads), gd, numel, out.data_ptr(),
+                                                  _stream(stream)), "fsdp_reduce_scatter_flat_noalloc")
 
 
 def _shard_len(h, rank):

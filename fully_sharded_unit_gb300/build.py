@@ -1,6 +1,6 @@
 """Build the in-tree CUDA library ``_lib/libfsdp_unit.so`` for sm_103a.
 
-Three translation units compiled in parallel with one ``-gencode`` each,
+Four translation units compiled in parallel with one ``-gencode`` each,
 then linked as a shared library whose only exported symbols are the C ABI
 of ``include/fsdp_unit.h``.  Rebuilds only when a source or header is newer
 than the library.
@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libfsdp_unit.so")
-SOURCES = ["plan.cpp", "kernels.cu", "api.cu"]
+SOURCES = ["plan.cpp", "kernels.cu", "api.cu", "noalloc.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",

@@ -61,6 +61,12 @@ bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) ==
 
 }  // namespace
 
+namespace fsdp {
+// The calling thread's failure reason for fsdp_last_error, for the entry
+// points defined outside this file.
+int record_error(int code, const std::string& why) { return fail(code, why); }
+}  // namespace fsdp
+
 struct fsdp_unit {
     int device = 0;
     Plan plan;

@@ -289,6 +289,47 @@ FSDP_API int fsdp_step(fsdp_unit* unit, const void* const* grads_dev, uint16_t* 
  * the bytes moved do.  Takes effect for calls enqueued afterwards. */
 FSDP_API int fsdp_unit_set_step_options(fsdp_unit* unit, int gather_source, int fuse_reduce_adamw);
 
+/* ---- reduce-scatter without device allocation ------------------------------ */
+/* Library infrastructure: the pages have no counterpart.
+ *
+ * Some callers cannot allocate device memory: a custom operator or plug-in
+ * inside a host framework that owns all of the GPU's memory through its own
+ * pool and forbids side allocations, or a process that has given nearly all
+ * of HBM to shards and optimizer state so that one more cudaMalloc would fail
+ * (and a cudaFree would stall every stream of the device).  Creating a unit
+ * allocates its arenas and work tables, so such a caller cannot use
+ * fsdp_reduce_scatter.  This entry point performs the same reduce-scatter for
+ * the FLAT layout with no unit and no allocation of any kind: the caller
+ * passes the inputs and the output, and the one scratch buffer it needs (the
+ * kernel's table of work tiles) is a fixed array in the library's device
+ * image, FSDP_NOALLOC_MAX_TILES tiles of 24 bytes (768 KiB), which every GPU
+ * that loads the library holds until the process exits.
+ *
+ * grads_dev: HOST array of num_ranks (1..1024) device pointers, each rank's
+ *   full gradient of `numel` elements of `grad_dtype` (F32 or BF16), 32-byte
+ *   aligned.
+ * out_dev: `numel` fp32 elements, 32-byte aligned: rank k's gradient shard is
+ *   written to out_dev[floor(k*numel/N) .. floor((k+1)*numel/N)), so the buffer
+ *   holds every rank's shard back to back, in rank order.  Each element is the
+ *   rank-order fp32 left fold divided by N, bit for bit what
+ *   fsdp_reduce_scatter writes for a FLAT unit of the same numel and N.
+ * Size limit: the work must fit the scratch, that is, the pieces of rank
+ *   ranges cut at multiples of 8192 elements number at most
+ *   FSDP_NOALLOC_MAX_TILES; numel <= 8192 * (32769 - num_ranks) always fits.
+ *   Larger sizes return FSDP_E_INVALID_ARG with the needed and available tile
+ *   counts in fsdp_last_error(), before anything is enqueued.
+ * The first call on each device looks up the scratch array's device address
+ *   (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ *   first call before any stream capture begins.
+ * Every call shares the one scratch table, and each call rewrites the part it
+ *   uses (a stream-ordered copy on `stream`, then the kernel), so calls in one
+ *   stream's order are safe; calls that may overlap on the GPU (other streams,
+ *   other threads, no ordering between them) race on the table and must not
+ *   be issued.  Errors: FSDP_E_INVALID_ARG, FSDP_E_ALIGN, FSDP_E_CUDA. */
+#define FSDP_NOALLOC_MAX_TILES 32768
+FSDP_API int fsdp_reduce_scatter_flat_noalloc(const void* const* grads_dev, int num_ranks, int grad_dtype,
+                                              int64_t numel, float* out_dev, void* stream);
+
 /* ---- state access (tests, checkpoint / resume) --------------------------- */
 /* Library infrastructure: the pages describe the sharded state ([FSDP] 3.2.1,
  * the FlatParameter owns its shards) but no access calls; these expose it per
