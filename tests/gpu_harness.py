@@ -7,14 +7,32 @@ elementwise (max abs err 1e-6 / max rel err 1e-5, read as an allclose bound);
 the harness also reports how many elements differ at all, since the kernel
 evaluates the same fp32 operation sequence as the oracle.
 
+AdamW's stricter per-state bounds are checked as well: v within a relative
+1e-5 everywhere (a sum of non-negative terms, no cancellation) and m within
+1e-5 x (beta1 |m_prev| + (1 - beta1) |g|) (the size of its operands).  The
+kernels evaluate the oracle's operation sequence, so the windowed checks at
+the full sizes also require AdamW state to be bit-identical (``bitwise``).
+
 Two modes:
 * full   -- every element, step by step (units the host holds easily);
 * window -- windows of global indices around every shard and parameter
-            boundary plus random windows.  Every operation after the layout is
-            elementwise in the global index, so the oracle computes a window
-            from the initial parameters and the ranks' gradients in that window.
+            boundary (+-4096) plus random windows, drawn afresh for every
+            step, each step's covering at least a given fraction of the unit
+            (5 % by default).  Every operation after the layout is elementwise
+            in the global index ("FSDP Architecture", the GPU-k boundary
+            formula and backward step 3; "PyTorch FSDP ...", section 3.2.1,
+            communication layout), so the oracle computes a window from the
+            initial parameters and the ranks' gradients in that window; the
+            union of all steps' windows is followed through every step and
+            compared at every step.  The oracle runs on slices of the union in
+            worker processes (spawned, so none inherits the CUDA context),
+            each calling the unchanged oracle functions; the split is exact
+            because every element is independent.
 """
 from __future__ import annotations
+
+import atexit
+import os
 
 import numpy as np
 import torch
@@ -54,16 +72,30 @@ def assert_bits_equal(got: np.ndarray, want: np.ndarray, what: str) -> None:
                              f"got {got[i]!r} want {want[i]!r}")
 
 
-def adamw_compare(got: np.ndarray, want: np.ndarray, what: str) -> dict:
-    g = got.astype(np.float64)
+def adamw_compare(got: np.ndarray, want: np.ndarray, what: str, which: str | None = None,
+                  m_prev: np.ndarray | None = None, g: np.ndarray | None = None, beta1: float = 0.9,
+                  bitwise: bool = False) -> dict:
+    """The AdamW tolerance on one state: |a - b| <= 1e-6 + 1e-5 |b| everywhere;
+    for v (which = "exp_avg_sq") also |a - b| <= 1e-5 |b|; for m (which =
+    "exp_avg", given the previous m and the last reduced gradient) also
+    |a - b| <= 1e-5 (beta1 |m_prev| + (1 - beta1) |g|).  With ``bitwise`` every
+    element must be bit-identical (NaN positions aside)."""
+    gv = got.astype(np.float64)
     w = want.astype(np.float64)
-    err = np.abs(g - w)
+    err = np.abs(gv - w)
     ok = err <= ATOL + RTOL * np.abs(w)
     nz = np.abs(w) > 0
     stats = dict(max_abs=float(err.max(initial=0.0)),
                  max_rel=float((err[nz] / np.abs(w[nz])).max(initial=0.0)),
                  n_diff=int((got.view(np.uint32) != want.view(np.uint32)).sum()), n=int(got.size))
     assert ok.all(), f"{what}: AdamW tolerance violated: {stats}"
+    if which == "exp_avg_sq":
+        assert (err <= RTOL * np.abs(w)).all(), f"{what}: v outside 1e-5 relative: {stats}"
+    if which == "exp_avg" and m_prev is not None and g is not None:
+        bound = RTOL * (beta1 * np.abs(m_prev.astype(np.float64)) + (1.0 - beta1) * np.abs(g.astype(np.float64)))
+        assert (err <= bound).all(), f"{what}: m outside its operand bound: {stats}"
+    if bitwise:
+        assert stats["n_diff"] == 0, f"{what}: not bit-identical to the oracle: {stats}"
     return stats
 
 
@@ -81,9 +113,25 @@ class Comparison:
         return sum(s["n_diff"] for s in self.adamw.values())
 
 
+def device_buffers(n: int, dtype, count: int, misalign: bool = False) -> list:
+    """`count` CUDA tensors of n elements; with ``misalign`` each is a view that
+    starts 16 bytes past a 32-byte boundary (16-byte but not 32-byte aligned)."""
+    if not misalign:
+        return [torch.empty(n, dtype=dtype, device="cuda") for _ in range(count)]
+    k = 16 // torch.empty((), dtype=dtype).element_size()
+    out = []
+    for _ in range(count):
+        base = torch.empty(n + 2 * k, dtype=dtype, device="cuda")
+        v = base[k:k + n] if base.data_ptr() % 32 == 0 else base[:n]
+        assert v.data_ptr() % 32 == 16
+        out.append(v)
+    return out
+
+
 def run_full(wl: workloads.Workload, unit: int = 0, use_step: bool = False, steps: int | None = None,
-             gen_device: str = "cpu", allocator=None) -> Comparison:
-    """Whole-unit comparison, every element, every step."""
+             gen_device: str = "cpu", allocator=None, misalign: bool = False) -> Comparison:
+    """Whole-unit comparison, every element, every step.  ``misalign``: the
+    gradients and the gathered outputs are only 16-byte aligned."""
     shapes = wl.shapes(unit)
     N, P = wl.N, wl.unit_numel(unit)
     steps = wl.steps if steps is None else steps
@@ -103,14 +151,16 @@ def run_full(wl: workloads.Workload, unit: int = 0, use_step: bool = False, step
         for k in range(N):   # shard-in
             assert_bits_equal(u.get_state("param", k).cpu().numpy(), orc.master[k], f"shard-in rank {k}")
             assert_bits_equal(u16(u.get_state("shadow", k)), orc.shadow[k], f"shadow rank {k}")
-        outs = [torch.empty(P, dtype=torch.int16, device="cuda") for _ in range(2)]
-        gdev = [torch.empty(P, dtype=wl.torch_grad_dtype(), device="cuda") for _ in range(wl.world)]
+        outs = device_buffers(P, torch.int16, 2, misalign)
+        gdev = device_buffers(P, wl.torch_grad_dtype(), wl.world, misalign)
         for s in range(steps):
             for r in range(wl.world):
                 if gen_device == "cuda":
                     workloads.grad_tensor(wl, unit, s, r, "cuda", out=gdev[r])
                 else:
                     gdev[r].copy_(workloads.grad_tensor(wl, unit, s, r, "cpu"))
+            if s == steps - 1:       # m before the last update, for m's operand bound
+                m_prev = [x.copy() for x in orc.m]
             want_outs = orc.step([grad_np(g) for g in gdev])
             if use_step:
                 u.step(gdev, outs[0], hp)
@@ -133,7 +183,9 @@ def run_full(wl: workloads.Workload, unit: int = 0, use_step: bool = False, step
         for k in range(N):
             for which, want in (("param", orc.master[k]), ("exp_avg", orc.m[k]), ("exp_avg_sq", orc.v[k])):
                 got = u.get_state(which, k).cpu().numpy()
-                cmp.add((which, k), adamw_compare(got, want, f"{which} rank {k}"))
+                cmp.add((which, k), adamw_compare(got, want, f"{which} rank {k}", which=which,
+                                                  m_prev=m_prev[k] if steps else None, g=orc.grad[k],
+                                                  beta1=hp["beta1"]))
             assert_bits_equal(u.get_state("grad", k).cpu().numpy(), orc.grad[k], f"final grad shard rank {k}")
             # the shadow is the cast of the GPU's own master (checked bitwise against that)
             assert_bits_equal(u16(u.get_state("shadow", k)), O.bf16_rne(u.get_state("param", k).cpu().numpy()),
@@ -144,24 +196,40 @@ def run_full(wl: workloads.Workload, unit: int = 0, use_step: bool = False, step
     return cmp
 
 
-def choose_windows(P: int, boundaries, half: int = 4096, n_random: int = 16, random_len: int = 1 << 16,
-                   seed: int = 0):
-    rng = np.random.default_rng(seed)
-    iv = [(max(0, b - half), min(P, b + half)) for b in boundaries]
-    for _ in range(n_random):
-        a = int(rng.integers(0, max(1, P - random_len)))
-        iv.append((a, min(P, a + random_len)))
-    iv.append((max(0, P - half), P))
-    iv.sort()
+def _merge(iv):
+    iv = sorted((a, b) for a, b in iv if b > a)
     merged = []
     for a, b in iv:
-        if b <= a:
-            continue
         if merged and a <= merged[-1][1]:
             merged[-1] = (merged[-1][0], max(merged[-1][1], b))
         else:
             merged.append((a, b))
     return merged
+
+
+def _covered(windows) -> int:
+    return sum(b - a for a, b in windows)
+
+
+def boundary_windows(P: int, boundaries, half: int = 4096):
+    """+-half elements around every boundary, and the last half elements."""
+    return _merge([(max(0, b - half), min(P, b + half)) for b in boundaries] + [(max(0, P - half), P)])
+
+
+def random_windows(P: int, frac: float, length: int, rng):
+    """Random windows of `length` elements (the last one shorter when needed)
+    whose union covers at least frac * P elements."""
+    want = min(P, int(np.ceil(frac * P)))
+    wins = []
+    while _covered(wins) < want:
+        need = want - _covered(wins)
+        n = max(1, need // length)
+        for _ in range(n):
+            ln = min(length, P)
+            a = int(rng.integers(0, P - ln + 1))
+            wins.append((a, a + ln))
+        wins = _merge(wins)
+    return wins
 
 
 def _window_index(windows) -> torch.Tensor:
@@ -181,17 +249,81 @@ def _flat_window(params, offsets, idx_np: np.ndarray) -> np.ndarray:
     return out
 
 
-def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None, n_random: int = 16,
-                 seed: int = 0, extra_boundaries=()) -> Comparison:
+# ---- the oracle on slices of a window, in spawned worker processes ----------
+
+_POOL = None
+
+
+def _oracle_pool():
+    """A pool of spawned workers (spawned: a forked child of a process that
+    holds a CUDA context can hang)."""
+    global _POOL
+    if _POOL is None:
+        import multiprocessing as mp
+        try:
+            n = len(os.sched_getaffinity(0))
+        except AttributeError:
+            n = os.cpu_count() or 1
+        _POOL = mp.get_context("spawn").Pool(max(1, min(16, n)))
+        atexit.register(_POOL.terminate)
+    return _POOL
+
+
+def _reduce_fn(kind):
+    if kind == "bf16":
+        return O.reduce_full_bf16
+    if isinstance(kind, tuple):          # ("hybrid", F)
+        return lambda gs: O.reduce_full_hybrid(gs, kind[1])
+    return O.reduce_full
+
+
+def _oracle_slice(args):
+    """The windowed cycle on one slice: O.run_window over all steps, and over
+    all but the last (for m before the last update)."""
+    p, g_steps, hp, kind = args
+    reduce = _reduce_fn(kind)
+    per_step, final = O.run_window(p, g_steps, O.AdamWHyper(**hp), reduce=reduce)
+    if len(g_steps) > 1:
+        _, (_, m_prev, _) = O.run_window(p, g_steps[:-1], O.AdamWHyper(**hp), reduce=reduce)
+    else:
+        m_prev = np.zeros_like(p)
+    return per_step, final, m_prev
+
+
+def oracle_windows(p_win, g_win, hp: dict, kind):
+    """O.run_window on the whole window, computed slice by slice in worker
+    processes; returns (per-step [(gathered, G)], (p, m, v), m_prev)."""
+    n = p_win.size
+    parts = max(1, min(64, n // (1 << 20)))
+    cuts = [n * i // parts for i in range(parts + 1)]
+    jobs = [(p_win[a:b], [[g[a:b] for g in gs] for gs in g_win], hp, kind) for a, b in zip(cuts, cuts[1:])]
+    res = _oracle_pool().map(_oracle_slice, jobs, chunksize=1) if parts > 1 else [_oracle_slice(jobs[0])]
+    steps = len(g_win)
+    per_step = [(np.concatenate([r[0][s][0] for r in res]), np.concatenate([r[0][s][1] for r in res]))
+                for s in range(steps)]
+    final = tuple(np.concatenate([r[1][i] for r in res]) for i in range(3))
+    m_prev = np.concatenate([r[2] for r in res])
+    return per_step, final, m_prev
+
+
+def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None, frac: float = 0.05,
+                 window_len: int = 1 << 20, seed: int = 0, extra_boundaries=(),
+                 bitwise: bool = True) -> Comparison:
     """Full-size unit through fsdp_step (the launch configuration the bench
-    times), compared on windows of global indices."""
+    times), compared on windows: +-4096 elements around every shard and
+    parameter boundary, plus, for every step, random windows drawn afresh
+    whose union is at least `frac` of the unit.  Every step's outputs
+    (gathered bf16 parameters, gradient shards) and the final master, m, v and
+    shadow are compared on the union of all of them.  ``cmp.covered`` is the
+    union's size; ``cmp.step_random`` each step's random coverage."""
     shapes = wl.shapes(unit)
     N, P = wl.N, wl.unit_numel(unit)
     steps = wl.steps if steps is None else steps
     hp = workloads.hyper(wl)
     lay = O.Layout(shapes, N, wl.layout)
     bounds = sorted({a for segs in lay.segments for a, _ in segs} | set(lay.offsets) | set(extra_boundaries))
-    windows = choose_windows(P, bounds, n_random=n_random, seed=seed)
+    rand = [random_windows(P, frac, window_len, np.random.default_rng([seed, unit, s])) for s in range(steps)]
+    windows = _merge(boundary_windows(P, bounds) + [w for r in rand for w in r])
     idx = _window_index(windows)
     idx_dev = idx.cuda()
     cmp = Comparison()
@@ -219,22 +351,20 @@ def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None
                  for w in ("param", "exp_avg", "exp_avg_sq")}
         shadow = np.concatenate([u16(u.read_global("shadow", a, b - a)) for a, b in windows])
         assert u.kernel_status() == 0, "a kernel raised its status word"
-        del gdev, out
+        del gdev, out, idx_dev
     finally:
         u.close()
-    if wl.replicas > 1:
-        def reduce(gs):
-            return O.reduce_full_hybrid(gs, N)
-    elif wl.reduce_dtype == "bf16":
-        reduce = O.reduce_full_bf16
-    else:
-        reduce = O.reduce_full
-    per_step, (p, m, v) = O.run_window(p_win, g_win, O.AdamWHyper(**hp), reduce=reduce)
+    kind = ("hybrid", N) if wl.replicas > 1 else ("bf16" if wl.reduce_dtype == "bf16" else "f32")
+    per_step, (p, m, v), m_prev = oracle_windows(p_win, g_win, hp, kind)
     for s, (gathered, G) in enumerate(per_step):
         assert_bits_equal(out_win[s], gathered, f"step {s} gathered (windows)")
         assert_bits_equal(gs_win[s], G, f"step {s} grad shard (windows)")
+    G_last = per_step[-1][1] if per_step else np.zeros_like(p)
     for which, want in (("param", p), ("exp_avg", m), ("exp_avg_sq", v)):
-        cmp.add(which, adamw_compare(final[which], want, f"{which} (windows)"))
+        cmp.add(which, adamw_compare(final[which], want, f"{which} (windows)", which=which, m_prev=m_prev,
+                                     g=G_last, beta1=hp["beta1"], bitwise=bitwise))
     assert_bits_equal(shadow, O.bf16_rne(final["param"]), "shadow (windows)")
     cmp.covered = int(idx.numel())
+    cmp.step_random = [_covered(r) for r in rand]
+    cmp.P = P
     return cmp

@@ -2,6 +2,8 @@
 allocator (here torch's caching allocator), the same results as with the
 library's own allocations, and every block handed back on success and on
 each failure path."""
+import gc
+
 import pytest
 import torch
 
@@ -27,6 +29,7 @@ def _lib():
 def test_torch_allocator_parity_and_accounting(name, use_step):
     wl = workloads.get(name)
     torch.cuda.synchronize()
+    gc.collect()          # tensors of earlier tests held in reference cycles would be freed mid-count
     base = torch.cuda.memory_allocated()
     alloc = B.TorchAllocator()
     cmp = H.run_full(wl, use_step=use_step, allocator=alloc)
@@ -39,6 +42,7 @@ def test_torch_allocator_parity_and_accounting(name, use_step):
 def test_torch_allocator_holds_the_arenas_while_the_unit_lives():
     wl = workloads.get("ragged_mini_flat_n7")
     alloc = B.TorchAllocator()
+    gc.collect()
     before = torch.cuda.memory_allocated()
     u = B.Unit(wl.shapes(0), "flat", wl.N, allocator=alloc)
     try:
