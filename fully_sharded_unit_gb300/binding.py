@@ -48,6 +48,7 @@ FSDP_KERNEL_REDUCE_ADAMW = 4
 FSDP_KERNEL_COUNT = 5
 
 FSDP_KSTATUS_WAIT_TIMEOUT = 1
+FSDP_KSTATUS_DRAIN_TIMEOUT = 2
 
 FSDP_NOALLOC_MAX_TILES = 32768
 
@@ -134,6 +135,7 @@ _SIGNATURES = {
     "fsdp_profile_read": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), _PI64]),
     "fsdp_profile_reset": (_I, [_P]),
     "fsdp_kernel_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
+    "fsdp_unit_set_wait_limit": (_I, [_P, ctypes.c_double, _I]),
     "fsdp_selftest_bounded_wait": (_I, [ctypes.c_double, ctypes.POINTER(ctypes.c_int32), _P]),
     "fsdp_host_device_pointer": (_I, [_P, ctypes.POINTER(_P)]),
     "fsdp_strerror": (ctypes.c_char_p, [_I]),
@@ -444,6 +446,11 @@ def fsdp_kernel_status(h, stream=None) -> int:
     return f.value
 
 
+def fsdp_unit_set_wait_limit(h, seconds=10.0, withhold_next=0) -> None:
+    """``withhold_next``: 0, 1 (one wait runs out) or 2 (the drain's wait too)."""
+    _check(lib().fsdp_unit_set_wait_limit(h, float(seconds), int(withhold_next)), "fsdp_unit_set_wait_limit")
+
+
 def fsdp_selftest_bounded_wait(limit_seconds=0.05, stream=None) -> bool:
     """True when a wait that nothing completes ran out and reported it."""
     t = ctypes.c_int32()
@@ -609,3 +616,6 @@ class Unit:
 
     def kernel_status(self, stream=None) -> int:
         return fsdp_kernel_status(self.handle, stream)
+
+    def set_wait_limit(self, seconds=10.0, withhold_next=0) -> None:
+        fsdp_unit_set_wait_limit(self.handle, seconds, withhold_next)

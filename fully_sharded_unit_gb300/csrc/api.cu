@@ -58,6 +58,7 @@ private:
 };
 
 bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
@@ -89,6 +90,10 @@ struct fsdp_unit {
     int64_t* step_counter = nullptr;
     int32_t* step_status = nullptr;
     int32_t* kstatus = nullptr;   // FSDP_KSTATUS_* bits raised by kernels
+    unsigned long long wait_ns = 0;   // bound of the staged kernels' waits (0: their 10 s default)
+    int withhold_next = 0;            // one-shot test of the give-up path (fsdp_unit_set_wait_limit)
+    bool needs_reload = false;        // a kernel gave up: state incomplete until fsdp_load_params
+    bool broken = false;              // a drain wait ran out too: only destroy is accepted
     float* master = nullptr;
     float* grad = nullptr;
     float* m = nullptr;
@@ -227,19 +232,42 @@ int check_hp(const fsdp_adamw_hp* hp) {
     return FSDP_OK;
 }
 
-int check_grads(const fsdp_unit* u, const void* const* grads) {
+// Gradient buffers must be 16-byte aligned; *narrow is set when one of them
+// is not 32-byte aligned (the kernels then use 16-byte loads).
+int check_grads(const fsdp_unit* u, const void* const* grads, int* narrow) {
     if (grads == nullptr) return fail(FSDP_E_INVALID_ARG, "grads array is null");
+    *narrow = 0;
     for (int r = 0; r < u->plan.N * u->replicas; ++r) {
         if (grads[r] == nullptr) return fail(FSDP_E_INVALID_ARG, "a gradient pointer is null");
-        if (!aligned32(grads[r])) return fail(FSDP_E_ALIGN, "a gradient buffer is not 32-byte aligned");
+        if (!aligned16(grads[r])) return fail(FSDP_E_ALIGN, "a gradient buffer is not 16-byte aligned");
+        if (!aligned32(grads[r])) *narrow = 1;
     }
     return FSDP_OK;
 }
 
+// The gathered output is written in 16-byte groups at 8-element boundaries.
 int check_out(const uint16_t* out) {
     if (out == nullptr) return fail(FSDP_E_INVALID_ARG, "output buffer is null");
-    if (!aligned32(out)) return fail(FSDP_E_ALIGN, "output buffer is not 32-byte aligned");
+    if (!aligned16(out)) return fail(FSDP_E_ALIGN, "output buffer is not 16-byte aligned");
     return FSDP_OK;
+}
+
+// Hot-path calls are refused after a kernel gave up (see fsdp_kernel_status).
+int check_usable(const fsdp_unit* u) {
+    if (u->broken)
+        return fail(FSDP_E_STATE, "a kernel's copies may have landed after it ended (FSDP_KSTATUS_DRAIN_TIMEOUT); "
+                                  "destroy the unit");
+    if (u->needs_reload)
+        return fail(FSDP_E_STATE, "a kernel gave up waiting (FSDP_KSTATUS_WAIT_TIMEOUT) and left the state "
+                                  "incomplete; reload it with fsdp_load_params");
+    return FSDP_OK;
+}
+
+// The staged kernels' wait bound and the one-shot give-up test, into `a`.
+void wait_args(fsdp_unit* u, fsdp::ReduceArgs* a) {
+    a->wait_ns = u->wait_ns;
+    a->withhold = u->withhold_next;
+    u->withhold_next = 0;
 }
 
 fsdp::AdamWConsts adamw_consts(const fsdp_adamw_hp* hp, int64_t t) {
@@ -294,13 +322,15 @@ int check_rs_options(const fsdp_rs_options* opt) {
     return FSDP_OK;
 }
 
-int enqueue_reduce_scatter(fsdp_unit* u, const void* const* grads, const fsdp_rs_options* opt,
+int enqueue_reduce_scatter(fsdp_unit* u, const void* const* grads, int narrow, const fsdp_rs_options* opt,
                            cudaStream_t st) {
     fsdp::ReduceArgs a{};
     a.F = u->plan.N;
     a.groups = u->replicas;
     a.bf16_reduce = u->reduce_dtype == FSDP_DTYPE_BF16 ? 1 : 0;
     a.inv_scale = 1.0f;
+    a.narrow = narrow;
+    wait_args(u, &a);
     if (opt != nullptr) {
         if (opt->inv_scale != 0.0 && opt->inv_scale != 1.0) {
             a.scale = 1;
@@ -318,13 +348,15 @@ int enqueue_reduce_scatter(fsdp_unit* u, const void* const* grads, const fsdp_rs
     });
 }
 
-int enqueue_reduce_adamw(fsdp_unit* u, const void* const* grads, const fsdp_adamw_hp* hp,
+int enqueue_reduce_adamw(fsdp_unit* u, const void* const* grads, int narrow, const fsdp_adamw_hp* hp,
                          cudaStream_t st) {
     fsdp::ReduceArgs a{};
     a.F = u->plan.N;
     a.groups = u->replicas;
     a.bf16_reduce = u->reduce_dtype == FSDP_DTYPE_BF16 ? 1 : 0;
     a.inv_scale = 1.0f;
+    a.narrow = narrow;
+    wait_args(u, &a);
     const fsdp::StepSource c = step_source(u, hp);
     int rc = profiled_launch(u, FSDP_KERNEL_REDUCE_ADAMW, st, "fused reduce-scatter + AdamW launch", [&] {
         return fsdp::launch_reduce_adamw(u->tiles, u->ntiles, grads, u->grad_dtype, a, u->grad, u->master,
@@ -377,6 +409,18 @@ int fsdp_kernel_status(fsdp_unit* u, int32_t* flags, void* stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "reading the kernel status word");
     *flags = v;
+    if (v & FSDP_KSTATUS_WAIT_TIMEOUT) u->needs_reload = true;
+    if (v & FSDP_KSTATUS_DRAIN_TIMEOUT) u->broken = true;
+    return FSDP_OK;
+}
+
+int fsdp_unit_set_wait_limit(fsdp_unit* u, double seconds, int withhold_next) {
+    int rc = check_unit(u, false);
+    if (rc) return rc;
+    if (!(seconds >= 1e-6 && seconds <= 60.0)) return fail(FSDP_E_INVALID_ARG, "seconds must be in [1e-6, 60]");
+    if (withhold_next < 0 || withhold_next > 2) return fail(FSDP_E_INVALID_ARG, "withhold_next must be 0, 1 or 2");
+    u->wait_ns = static_cast<unsigned long long>(seconds * 1e9);
+    u->withhold_next = withhold_next;
     return FSDP_OK;
 }
 
@@ -539,6 +583,7 @@ int fsdp_unit_destroy(fsdp_unit* u) {
 int fsdp_load_params(fsdp_unit* u, const float* const* params, void* stream) {
     int rc = check_unit(u, false);
     if (rc) return rc;
+    if (u->broken) return check_usable(u);
     if (params == nullptr) return fail(FSDP_E_INVALID_ARG, "params array is null");
     std::vector<fsdp::ParamSrc> src(u->nparams);
     for (int p = 0; p < u->nparams; ++p) {
@@ -569,11 +614,13 @@ int fsdp_load_params(fsdp_unit* u, const float* const* params, void* stream) {
     u->t = 0;
     u->device_steps = false;
     u->loaded = true;
+    u->needs_reload = false;
     return FSDP_OK;
 }
 
 int fsdp_allgather(fsdp_unit* u, uint16_t* out, void* stream) {
     int rc = check_unit(u, true);
+    if (rc == FSDP_OK) rc = check_usable(u);
     if (rc == FSDP_OK) rc = check_out(out);
     if (rc) return rc;
     DeviceGuard dg(u->device);
@@ -582,27 +629,32 @@ int fsdp_allgather(fsdp_unit* u, uint16_t* out, void* stream) {
 }
 
 int fsdp_reduce_scatter(fsdp_unit* u, const void* const* grads, void* stream) {
+    int narrow = 0;
     int rc = check_unit(u, true);
-    if (rc == FSDP_OK) rc = check_grads(u, grads);
+    if (rc == FSDP_OK) rc = check_usable(u);
+    if (rc == FSDP_OK) rc = check_grads(u, grads, &narrow);
     if (rc) return rc;
     DeviceGuard dg(u->device);
     if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
-    return enqueue_reduce_scatter(u, grads, nullptr, static_cast<cudaStream_t>(stream));
+    return enqueue_reduce_scatter(u, grads, narrow, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 int fsdp_reduce_scatter_ex(fsdp_unit* u, const void* const* grads, const fsdp_rs_options* opt,
                            void* stream) {
+    int narrow = 0;
     int rc = check_unit(u, true);
-    if (rc == FSDP_OK) rc = check_grads(u, grads);
+    if (rc == FSDP_OK) rc = check_usable(u);
+    if (rc == FSDP_OK) rc = check_grads(u, grads, &narrow);
     if (rc == FSDP_OK) rc = check_rs_options(opt);
     if (rc) return rc;
     DeviceGuard dg(u->device);
     if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
-    return enqueue_reduce_scatter(u, grads, opt, static_cast<cudaStream_t>(stream));
+    return enqueue_reduce_scatter(u, grads, narrow, opt, static_cast<cudaStream_t>(stream));
 }
 
 int fsdp_zero_grad(fsdp_unit* u, void* stream) {
     int rc = check_unit(u, true);
+    if (rc == FSDP_OK) rc = check_usable(u);
     if (rc) return rc;
     DeviceGuard dg(u->device);
     if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
@@ -613,6 +665,7 @@ int fsdp_zero_grad(fsdp_unit* u, void* stream) {
 
 int fsdp_adamw_step(fsdp_unit* u, const fsdp_adamw_hp* hp, void* stream) {
     int rc = check_unit(u, true);
+    if (rc == FSDP_OK) rc = check_usable(u);
     if (rc == FSDP_OK) rc = check_hp(hp);
     if (rc) return rc;
     DeviceGuard dg(u->device);
@@ -622,9 +675,11 @@ int fsdp_adamw_step(fsdp_unit* u, const fsdp_adamw_hp* hp, void* stream) {
 
 int fsdp_step(fsdp_unit* u, const void* const* grads, uint16_t* out, const fsdp_adamw_hp* hp,
               void* stream) {
+    int narrow = 0;
     int rc = check_unit(u, true);
+    if (rc == FSDP_OK) rc = check_usable(u);
     if (rc == FSDP_OK) rc = check_out(out);
-    if (rc == FSDP_OK) rc = check_grads(u, grads);
+    if (rc == FSDP_OK) rc = check_grads(u, grads, &narrow);
     if (rc == FSDP_OK) rc = check_hp(hp);
     if (rc) return rc;
     DeviceGuard dg(u->device);
@@ -632,8 +687,8 @@ int fsdp_step(fsdp_unit* u, const void* const* grads, uint16_t* out, const fsdp_
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     rc = enqueue_gather(u, out, st);                       // forward
     if (rc == FSDP_OK && u->raf) rc = enqueue_gather(u, out, st);   // backward re-gather
-    if (rc == FSDP_OK && u->fuse) return enqueue_reduce_adamw(u, grads, hp, st);
-    if (rc == FSDP_OK) rc = enqueue_reduce_scatter(u, grads, nullptr, st);
+    if (rc == FSDP_OK && u->fuse) return enqueue_reduce_adamw(u, grads, narrow, hp, st);
+    if (rc == FSDP_OK) rc = enqueue_reduce_scatter(u, grads, narrow, nullptr, st);
     if (rc == FSDP_OK) rc = enqueue_adamw(u, hp, st);
     return rc;
 }

@@ -9,6 +9,9 @@
 // (ld/st .v8.f32) or one 128-bit bf16 access (.v4.b32); the plain
 // bf16-gradient reduce-scatter reads 16-element groups, one 256-bit access
 // per rank; the staged fused kernel moves whole chunk rows with cp.async.bulk.
+// Gradient buffers that are only 16-byte aligned take the NARROW instances of
+// the register-staged reductions: fp32 groups load as two 128-bit halves and
+// the plain bf16 reduce-scatter falls back to 8-element (128-bit) groups.
 // Segment-driven kernels walk a tile table (see plan.hpp): a tile never spans
 // two segments, and because arena slots are congruent to global indices
 // modulo 32 elements, a group that is aligned in the unsharded buffer is
@@ -52,6 +55,19 @@ __device__ __forceinline__ F8 ld8_ro(const float* p) {
         : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]), "=f"(r.v[5]),
           "=f"(r.v[6]), "=f"(r.v[7])
         : "l"(p));
+    return r;
+}
+
+// The same eight values as two 128-bit accesses, for buffers that are only
+// 16-byte aligned.
+__device__ __forceinline__ F8 ld8_ro_narrow(const float* p) {
+    F8 r;
+    asm("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+        : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3])
+        : "l"(p));
+    asm("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+        : "=f"(r.v[4]), "=f"(r.v[5]), "=f"(r.v[6]), "=f"(r.v[7])
+        : "l"(p + 4));
     return r;
 }
 
@@ -285,8 +301,11 @@ struct GradIO<float> {
     struct Group {
         F8 f;
     };
+    // NARROW: the gradient buffers may be only 16-byte aligned
+    template <bool NARROW>
     static __device__ __forceinline__ Group load8(const void* base, int64_t i) {
-        return Group{ld8_ro(static_cast<const float*>(base) + i)};
+        if constexpr (NARROW) return Group{ld8_ro_narrow(static_cast<const float*>(base) + i)};
+        else return Group{ld8_ro(static_cast<const float*>(base) + i)};
     }
     static __device__ __forceinline__ void widen(const Group& g, F8& out) { out = g.f; }
     // the group rounded to bf16 pairs (RNE), for the bf16 reduction
@@ -304,6 +323,8 @@ struct GradIO<uint16_t> {
     struct Group {
         uint4 w;
     };
+    // one 16-byte access: needs 16-byte alignment either way
+    template <bool NARROW>
     static __device__ __forceinline__ Group load8(const void* base, int64_t i) {
         return Group{ld8bf_ro(static_cast<const uint16_t*>(base) + i)};
     }
@@ -376,7 +397,8 @@ __device__ __forceinline__ void finish_bf16(const BGroup<W>& acc, float fW, F8* 
 }
 
 // Eight consecutive elements (an aligned group), same order of operations.
-template <typename GT, int NMAX, bool BF16>
+// NARROW: 16-byte instead of 32-byte fp32 gradient loads.
+template <typename GT, int NMAX, bool BF16, bool NARROW = false>
 __device__ __forceinline__ F8 reduce8(const GradPtrs<NMAX>& gp, const ReduceArgs& a, int groups,
                                       float fW, int64_t gi) {
     using IO = GradIO<GT>;
@@ -387,7 +409,7 @@ __device__ __forceinline__ F8 reduce8(const GradPtrs<NMAX>& gp, const ReduceArgs
             typename IO::Group x[kBatch];
 #pragma unroll
             for (int b = 0; b < kBatch; ++b)
-                if (r0 + b < a.F) x[b] = IO::load8(gp.p[r0 + b], gi);
+                if (r0 + b < a.F) x[b] = IO::template load8<NARROW>(gp.p[r0 + b], gi);
 #pragma unroll
             for (int b = 0; b < kBatch; ++b) {
                 if (r0 + b < a.F) {
@@ -407,7 +429,7 @@ __device__ __forceinline__ F8 reduce8(const GradPtrs<NMAX>& gp, const ReduceArgs
                 typename IO::Group x[kBatch];
 #pragma unroll
                 for (int b = 0; b < kBatch; ++b)
-                    if (r0 + b < a.F) x[b] = IO::load8(gp.p[base + r0 + b], gi);
+                    if (r0 + b < a.F) x[b] = IO::template load8<NARROW>(gp.p[base + r0 + b], gi);
 #pragma unroll
                 for (int b = 0; b < kBatch; ++b) {
                     if (r0 + b < a.F) {
@@ -538,8 +560,9 @@ __device__ __forceinline__ void post8(F8& x, const float* dst, bool post, const 
 
 // EXT = false compiles the plain reduce-scatter (one group, no unscale, no
 // accumulation, no flag) with the fewest registers; EXT = true adds hybrid
-// groups and the post-reduction options.
-template <typename GT, int NMAX, bool BF16, bool EXT>
+// groups and the post-reduction options.  NARROW = true serves gradient
+// buffers that are only 16-byte aligned: 16-byte loads throughout.
+template <typename GT, int NMAX, bool BF16, bool EXT, bool NARROW>
 __global__ void __launch_bounds__(kBlock) reduce_scatter_kernel(const Tile* __restrict__ tiles,
                                                                 int64_t ntiles, GradPtrs<NMAX> gp,
                                                                 ReduceArgs a, float* __restrict__ gshard) {
@@ -556,7 +579,7 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_kernel(const Tile* __re
     // 128 registers (2 CTAs per SM), the 8-wide one 78 (3 CTAs per SM), which
     // measured 9.44 ms against 9.73 ms for two replication groups and 6.10 ms
     // against 6.53 ms per accumulated micro-batch.
-    constexpr int A = (std::is_same<GT, uint16_t>::value && !EXT) ? 16 : 8;
+    constexpr int A = (std::is_same<GT, uint16_t>::value && !EXT && !NARROW) ? 16 : 8;
     bool bad = false;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const Tile tl = tiles[t];
@@ -585,7 +608,7 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_kernel(const Tile* __re
                 st8(d, x0);
                 st8(d + 8, x1);
             } else {
-                F8 x = reduce8<GT, NMAX, BF16>(gp, a, groups, fW, g0 + 8 * static_cast<int64_t>(v));
+                F8 x = reduce8<GT, NMAX, BF16, NARROW>(gp, a, groups, fW, g0 + 8 * static_cast<int64_t>(v));
                 post8(x, d, post, a, found != nullptr, bad);
                 st8(d, x);
             }
@@ -668,7 +691,7 @@ __global__ void __launch_bounds__(kBlock) adamw_kernel(int64_t n8, float* __rest
 // 12.35 ms against 13.24 ms uncapped.  Same operation sequence as the two
 // separate kernels, so the results are identical; only segment elements are
 // touched (pads stay zero, which AdamW would preserve anyway).
-template <typename GT, int NMAX, bool BF16, bool HYBRID>
+template <typename GT, int NMAX, bool BF16, bool HYBRID, bool NARROW>
 __global__ void __launch_bounds__(kBlock, sizeof(GT) == 2 ? 3 : 2) reduce_adamw_kernel(const Tile* __restrict__ tiles,
                                                               int64_t ntiles, GradPtrs<NMAX> gp,
                                                               ReduceArgs a, float* __restrict__ gshard,
@@ -698,7 +721,7 @@ __global__ void __launch_bounds__(kBlock, sizeof(GT) == 2 ? 3 : 2) reduce_adamw_
         }
 #pragma unroll 1
         for (int vi = tid; vi < sp.nvec; vi += kBlock) {
-            const F8 G = reduce8<GT, NMAX, BF16>(gp, a, groups, fW, g0 + 8 * static_cast<int64_t>(vi));
+            const F8 G = reduce8<GT, NMAX, BF16, NARROW>(gp, a, groups, fW, g0 + 8 * static_cast<int64_t>(vi));
             st8(gshard + s0 + 8 * static_cast<int64_t>(vi), G);
             float4* slot = reinterpret_cast<float4*>(gsm + 8 * vi);
             slot[0] = make_float4(G.v[0], G.v[1], G.v[2], G.v[3]);
@@ -761,10 +784,15 @@ __host__ __device__ constexpr int chunk_for(int elem_bytes) {   // stage bytes p
          : 1024 * elem_bytes <= kStageMaxBytes ? 1024
          : 512 * elem_bytes <= kStageMaxBytes ? 512 : 0;
 }
-// A wait on a stage gives up after this long: the kernel then raises bit
-// FSDP_KSTATUS_WAIT_TIMEOUT of the unit's status word, waits (again bounded)
-// for its own copies in flight and returns.
+// A wait on a stage gives up after ReduceArgs::wait_ns (this default when 0):
+// the kernel then raises bit FSDP_KSTATUS_WAIT_TIMEOUT of the unit's status
+// word, waits (again bounded) for its own copies in flight, raising
+// FSDP_KSTATUS_DRAIN_TIMEOUT if one of those waits runs out too, and returns.
 constexpr unsigned long long kWaitLimitNs = 10000000000ull;
+
+__device__ __forceinline__ unsigned long long wait_limit(const ReduceArgs& a) {
+    return a.wait_ns != 0 ? a.wait_ns : kWaitLimitNs;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -939,6 +967,8 @@ __global__ void __launch_bounds__(kBlock) reduce_adamw_bulk_kernel(const Tile* _
     Body pb{};
     bool pb_valid = false;
     uint32_t issued = 0, consumed = 0;
+    uint32_t withheld = 0xFFFFFFFFu;   // the stage armed without copies (a.withhold), if any
+    const unsigned long long limit = wait_limit(a);
     auto top_up = [&]() {
         while (issued - consumed < static_cast<uint32_t>(kStages) && pt < ntiles) {
             if (!pb_valid) {
@@ -957,13 +987,17 @@ __global__ void __launch_bounds__(kBlock) reduce_adamw_bulk_kernel(const Tile* _
             const int s = static_cast<int>(issued % kStages);
             unsigned char* st = ring + s * sbytes;
             mbar_expect_tx(&full[s], n * static_cast<uint32_t>(W * sizeof(GT) + 12));
-            for (int r = 0; r < W; ++r)
-                bulk_g2s(st + static_cast<size_t>(r) * CH * sizeof(GT),
-                         static_cast<const GT*>(gp.p[r]) + pb.ga + off, n * sizeof(GT), &full[s]);
-            unsigned char* pmv = st + static_cast<size_t>(W) * CH * sizeof(GT);
-            bulk_g2s(pmv, p + pb.sa + off, n * 4, &full[s]);
-            bulk_g2s(pmv + CH * 4, m + pb.sa + off, n * 4, &full[s]);
-            bulk_g2s(pmv + 2 * CH * 4, v + pb.sa + off, n * 4, &full[s]);
+            if (a.withhold != 0 && blockIdx.x == 0 && issued == 0) {
+                withheld = issued;   // nothing will complete this stage: its wait runs out
+            } else {
+                for (int r = 0; r < W; ++r)
+                    bulk_g2s(st + static_cast<size_t>(r) * CH * sizeof(GT),
+                             static_cast<const GT*>(gp.p[r]) + pb.ga + off, n * sizeof(GT), &full[s]);
+                unsigned char* pmv = st + static_cast<size_t>(W) * CH * sizeof(GT);
+                bulk_g2s(pmv, p + pb.sa + off, n * 4, &full[s]);
+                bulk_g2s(pmv + CH * 4, m + pb.sa + off, n * 4, &full[s]);
+                bulk_g2s(pmv + 2 * CH * 4, v + pb.sa + off, n * 4, &full[s]);
+            }
             ++issued;
             ++pc;
         }
@@ -993,7 +1027,7 @@ __global__ void __launch_bounds__(kBlock) reduce_adamw_bulk_kernel(const Tile* _
             if (tid == 0) top_up();
             const int s = static_cast<int>(consumed % kStages);
             const uint32_t parity = (consumed / kStages) & 1u;
-            const bool got = mbar_wait(&full[s], parity);
+            const bool got = mbar_wait(&full[s], parity, limit);
             const int64_t off = ch * CH;
             const int64_t n = b.n - off < CH ? b.n - off : CH;
             for (int e = tid * 4; got && e < n; e += 4 * kBlock) {
@@ -1023,10 +1057,15 @@ __global__ void __launch_bounds__(kBlock) reduce_adamw_bulk_kernel(const Tile* _
     }
     if (!ok) {
         // a copy did not arrive in time: report, wait (bounded) for the copies
-        // this CTA still has in flight, and leave
+        // this CTA still has in flight, and leave; a drain wait that runs out
+        // too means copies may still land in this SM's shared memory
         if (tid == 0) {
             atomicOr(wait_status, FSDP_KSTATUS_WAIT_TIMEOUT);
-            for (uint32_t q = consumed - 1; q < issued; ++q) mbar_wait(&full[q % kStages], (q / kStages) & 1u);
+            for (uint32_t q = consumed - 1; q < issued; ++q) {
+                if (q == withheld && a.withhold == 1) continue;   // armed, but no copy was issued
+                if (!mbar_wait(&full[q % kStages], (q / kStages) & 1u, limit))
+                    atomicOr(wait_status, FSDP_KSTATUS_DRAIN_TIMEOUT);
+            }
         }
         __syncthreads();
     }
@@ -1073,6 +1112,8 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_bulk_kernel(const Tile*
     Body pb{};
     bool pb_valid = false;
     uint32_t issued = 0, consumed = 0;
+    uint32_t withheld = 0xFFFFFFFFu;   // the stage armed without copies (a.withhold), if any
+    const unsigned long long limit = wait_limit(a);
     auto top_up = [&]() {
         while (issued - consumed < static_cast<uint32_t>(S) && pt < ntiles) {
             if (!pb_valid) {
@@ -1091,10 +1132,14 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_bulk_kernel(const Tile*
             const int s = static_cast<int>(issued % S);
             unsigned char* st = ring + s * sbytes;
             mbar_expect_tx(&full[s], n * elem_bytes);
-            for (int r = 0; r < W; ++r)
-                bulk_g2s(st + static_cast<size_t>(r) * CH * sizeof(GT),
-                         static_cast<const GT*>(gp.p[r]) + pb.ga + off, n * sizeof(GT), &full[s]);
-            if (acc) bulk_g2s(st + rows_bytes, gshard + pb.sa + off, n * 4, &full[s]);
+            if (a.withhold != 0 && blockIdx.x == 0 && issued == 0) {
+                withheld = issued;   // nothing will complete this stage: its wait runs out
+            } else {
+                for (int r = 0; r < W; ++r)
+                    bulk_g2s(st + static_cast<size_t>(r) * CH * sizeof(GT),
+                             static_cast<const GT*>(gp.p[r]) + pb.ga + off, n * sizeof(GT), &full[s]);
+                if (acc) bulk_g2s(st + rows_bytes, gshard + pb.sa + off, n * 4, &full[s]);
+            }
             ++issued;
             ++pc;
         }
@@ -1120,7 +1165,7 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_bulk_kernel(const Tile*
             if (tid == 0) top_up();
             const int s = static_cast<int>(consumed % S);
             const uint32_t parity = (consumed / S) & 1u;
-            const bool got = mbar_wait(&full[s], parity);
+            const bool got = mbar_wait(&full[s], parity, limit);
             const int64_t off = ch * CH;
             const int64_t n = b.n - off < CH ? b.n - off : CH;
             for (int e = tid * 4; got && e < n; e += 4 * kBlock) {
@@ -1150,7 +1195,10 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_bulk_kernel(const Tile*
     }
     if (!ok && tid == 0) {
         atomicOr(kstatus, FSDP_KSTATUS_WAIT_TIMEOUT);
-        for (uint32_t q = consumed - 1; q < issued; ++q) mbar_wait(&full[q % S], (q / S) & 1u);
+        for (uint32_t q = consumed - 1; q < issued; ++q) {
+            if (q == withheld && a.withhold == 1) continue;   // armed, but no copy was issued
+            if (!mbar_wait(&full[q % S], (q / S) & 1u, limit)) atomicOr(kstatus, FSDP_KSTATUS_DRAIN_TIMEOUT);
+        }
     }
     if (__syncthreads_or(bad) && tid == 0 && a.found != nullptr) *a.found = 1;
 }
@@ -1296,7 +1344,15 @@ static cudaError_t launch_rs_t(const Tile* tiles, int64_t ntiles, const void* co
             if (sp.chunk == 512) return launch_rs_bulk<GT, NMAX, BF16, 512, 2>(tiles, ntiles, gp, a, gshard, kstatus, st);
         }
     }
-    return launch_pdl(reduce_scatter_kernel<GT, NMAX, BF16, EXT>, grid_for(ntiles), kBlock, st, tiles, ntiles,
+    // 16-byte-aligned gradients: fp32 groups load as two 16-byte halves, and
+    // the plain bf16 form drops from 16-wide (32-byte) to 8-wide groups; the
+    // extended bf16 form already loads 16 bytes at a time
+    if constexpr (std::is_same<GT, float>::value || !EXT) {
+        if (a.narrow)
+            return launch_pdl(reduce_scatter_kernel<GT, NMAX, BF16, EXT, true>, grid_for(ntiles), kBlock, st, tiles,
+                              ntiles, gp, a, gshard);
+    }
+    return launch_pdl(reduce_scatter_kernel<GT, NMAX, BF16, EXT, false>, grid_for(ntiles), kBlock, st, tiles, ntiles,
                       gp, a, gshard);
 }
 
@@ -1376,10 +1432,19 @@ static cudaError_t launch_ra_t(const Tile* tiles, int64_t ntiles, const void* co
                                                          kstatus, st);
         }
     }
+    if constexpr (std::is_same<GT, float>::value) {   // 16-byte-aligned fp32 gradients
+        if (a.narrow) {
+            if (a.groups > 1)
+                return launch_pdl(reduce_adamw_kernel<GT, NMAX, BF16, true, true>, grid_for(ntiles), kBlock, st,
+                                  tiles, ntiles, gp, a, gshard, p, m, v, shadow, c);
+            return launch_pdl(reduce_adamw_kernel<GT, NMAX, BF16, false, true>, grid_for(ntiles), kBlock, st,
+                              tiles, ntiles, gp, a, gshard, p, m, v, shadow, c);
+        }
+    }
     if (a.groups > 1)
-        return launch_pdl(reduce_adamw_kernel<GT, NMAX, BF16, true>, grid_for(ntiles), kBlock, st, tiles,
+        return launch_pdl(reduce_adamw_kernel<GT, NMAX, BF16, true, false>, grid_for(ntiles), kBlock, st, tiles,
                           ntiles, gp, a, gshard, p, m, v, shadow, c);
-    return launch_pdl(reduce_adamw_kernel<GT, NMAX, BF16, false>, grid_for(ntiles), kBlock, st, tiles,
+    return launch_pdl(reduce_adamw_kernel<GT, NMAX, BF16, false, false>, grid_for(ntiles), kBlock, st, tiles,
                       ntiles, gp, a, gshard, p, m, v, shadow, c);
 }
 

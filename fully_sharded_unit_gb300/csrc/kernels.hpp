@@ -44,6 +44,12 @@ struct ReduceArgs {
     int scale;
     int accumulate;     // add into the existing gradient shard
     int32_t* found;     // set to 1 when a written value is not finite; may be null
+    int narrow;         // 1: some gradient buffer is only 16-byte aligned (16-byte loads)
+    unsigned long long wait_ns;   // bound of each wait in the staged kernels (0: 10 s)
+    int withhold;       // test of the give-up path: CTA 0 of a staged kernel arms its
+                        // first stage's barrier but issues none of that stage's copies;
+                        // 1: the drain skips that stage, 2: the drain waits for it too
+                        // (and runs out: no copy is in flight, nothing lands late)
 };
 
 cudaError_t launch_shard_in(const Tile* tiles, int64_t ntiles, const ParamSrc* params,

@@ -25,9 +25,11 @@
  *  - Pointers named *_dev are device pointers (or managed memory) that the
  *    caller owns and keeps alive until the enqueued work has finished.  The
  *    library never keeps a caller pointer after a call returns.
- *  - Hot-path buffers (gradients, the gathered output) must be 32-byte
- *    aligned (FSDP_E_ALIGN otherwise); allocations from cudaMalloc or torch
- *    always are.
+ *  - Hot-path buffers (gradients, the gathered output) must be 16-byte
+ *    aligned (FSDP_E_ALIGN otherwise).  Gradients that are all 32-byte aligned
+ *    (as allocations from cudaMalloc or torch are) are read with 32-byte
+ *    vector loads; if any is only 16-byte aligned, that call's reduction
+ *    reads every gradient with 16-byte loads (same results).
  *  - Element types: fp32 is IEEE binary32; bf16 is stored as uint16_t bit
  *    patterns (the upper half of the binary32 pattern).
  *  - A unit is not thread-safe; distinct units are independent.
@@ -54,7 +56,7 @@ extern "C" {
 #define FSDP_E_OOM         (-2)  /* device or host allocation failed        */
 #define FSDP_E_CUDA        (-3)  /* a CUDA runtime call or launch failed    */
 #define FSDP_E_STATE       (-4)  /* call not valid in the unit's state      */
-#define FSDP_E_ALIGN       (-5)  /* a buffer is not 32-byte aligned         */
+#define FSDP_E_ALIGN       (-5)  /* a buffer is not aligned as required     */
 #define FSDP_E_CAPACITY    (-6)  /* caller's output array is too small      */
 
 /* ---- enums ------------------------------------------------------------ */
@@ -100,6 +102,10 @@ extern "C" {
 /* bits of a unit's kernel status word (fsdp_kernel_status) */
 #define FSDP_KSTATUS_WAIT_TIMEOUT  1   /* a kernel gave up waiting for its own copies into
                                           shared memory; its outputs are incomplete      */
+#define FSDP_KSTATUS_DRAIN_TIMEOUT 2   /* after that, a wait for its remaining copies ran out
+                                          too: copies may have landed in shared memory after
+                                          the kernel ended, so nothing computed around that
+                                          launch can be trusted                             */
 
 /* ---- plain structs ------------------------------------------------------ */
 typedef struct fsdp_unit fsdp_unit;   /* opaque; one FlatParamHandle ([FSDP] section 4.2) */
@@ -268,7 +274,10 @@ FSDP_API int fsdp_zero_grad(fsdp_unit* unit, void* stream);
  *     v = fp32(beta2)*v + fp32(1-beta2)*(g*g)
  *     p = p - fp32(lr/(1-beta1^t)) * (m / (sqrt(v / fp32(1-beta2^t)) + fp32(eps)))
  *     shadow = RNE_bf16(p)
- * The scalar constants are formed in double on the host and rounded once. */
+ * The scalar constants are formed in double on the host and rounded once.
+ * The step count advances when the launch is enqueued; if a kernel of this
+ * unit later reports a status bit (fsdp_kernel_status), the count no longer
+ * matches the state and the unit must be reloaded. */
 FSDP_API int fsdp_adamw_step(fsdp_unit* unit, const fsdp_adamw_hp* hp, void* stream);
 
 /* One unit step ([ARCH] the per-unit cycle; [FSDP] section 5.4): gather into
@@ -278,7 +287,8 @@ FSDP_API int fsdp_adamw_step(fsdp_unit* unit, const fsdp_adamw_hp* hp, void* str
  * fuse_reduce_adamw the last two run as one kernel with the same results;
  * when W x gradient bytes <= 100 (bf16 gradients with W <= 50, fp32 with
  * W <= 25) that kernel stages its inputs in shared memory with bounded waits
- * (see fsdp_kernel_status). */
+ * (see fsdp_kernel_status: a raised bit means this step's update was
+ * incomplete while the step count advanced, and the unit must be reloaded). */
 FSDP_API int fsdp_step(fsdp_unit* unit, const void* const* grads_dev, uint16_t* out_bf16_dev,
               const fsdp_adamw_hp* hp, void* stream);
 
@@ -414,8 +424,32 @@ FSDP_API int fsdp_memory_report(const fsdp_unit* unit, int rank, int64_t* param_
  * that runs out raises a FSDP_KSTATUS_* bit in the unit's device status word,
  * and the kernel returns with its outputs incomplete instead of hanging.
  * fsdp_kernel_status synchronises `stream`, stores the word in *flags
- * (0: nothing raised) and clears it.  The word starts at 0 at creation. */
+ * (0: nothing raised) and clears it.  The word starts at 0 at creation.
+ * Reading a raised bit also blocks the unit: after FSDP_KSTATUS_WAIT_TIMEOUT
+ * the gradient shards, master, m and v may be partly updated and the step
+ * count has advanced past an incomplete update, so fsdp_allgather,
+ * fsdp_reduce_scatter(_ex), fsdp_zero_grad, fsdp_adamw_step and fsdp_step
+ * return FSDP_E_STATE until fsdp_load_params reloads the unit; after
+ * FSDP_KSTATUS_DRAIN_TIMEOUT every call but fsdp_unit_destroy and the
+ * read-only queries is refused (destroy and recreate the unit).  Calls
+ * enqueued before the word is read are not refused: read it before trusting
+ * any result that followed the launch in question. */
 FSDP_API int fsdp_kernel_status(fsdp_unit* unit, int32_t* flags, void* stream);
+
+/* Library infrastructure (the pages have no counterpart).
+ * The bound of every wait of this unit's staged kernels: `seconds` in
+ * [1e-6, 60] (10 s until set).  withhold_next arms a one-shot test of the
+ * give-up path (0: none): in the next reduce-scatter or fused fsdp_step
+ * launch of this unit, if it is one of the shared-memory staged kernels,
+ * CTA 0 arms the barrier of its first stage but issues none of that stage's
+ * copies, so that wait runs out exactly as for a copy that never arrives.
+ * With 1 the kernel raises FSDP_KSTATUS_WAIT_TIMEOUT, waits for its other
+ * copies and returns with its outputs incomplete; with 2 its drain also
+ * waits on the withheld stage, runs out again and raises
+ * FSDP_KSTATUS_DRAIN_TIMEOUT as well (no copy is in flight, so nothing lands
+ * late).  The launch touches no memory a normal launch would not (it reads
+ * and writes less).  The next launch of either kind consumes the request. */
+FSDP_API int fsdp_unit_set_wait_limit(fsdp_unit* unit, double seconds, int withhold_next);
 
 /* Library infrastructure (the pages have no counterpart).
  * Self-test of the bounded wait on the current device: one CTA waits on an
