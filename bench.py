@@ -14,8 +14,14 @@ unit step, every required read and write once:
     reduce-sc.  N*g_b*P read (N gradients) + 4P write (fp32 shards)
     AdamW       16P read (p, g, m, v) + 12P write (p, m, v) + 2P (bf16 shadow)
 
+The line also carries the same step counted the survey's way, without the
+bf16 shadow write ((44 + N*g_b)P per unit, "value_survey"), the oracle's
+throughput on the host cores (all cores and one), and a "configs" object with
+every other workload's model step timed the same way.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload NAME] [--e2e-steps E] [--no-e2e] [--no-cpu-baseline]
+                       [--no-configs]
 With --gpus N > 1 (under torchrun) every rank runs an independent replica of
 the workload on its own GPU (the N virtual ranks of a unit never span GPUs);
 value = all ranks' counted bytes / the slowest rank's time.
@@ -60,6 +66,20 @@ def counted_bytes(wl: workloads.Workload, unit: int) -> dict:
     step = R * gather + (reduce_adamw if wl.fuse_reduce_adamw else rs + adamw)
     return dict(gather=gather, reduce_scatter=rs, adamw=adamw, reduce_adamw=reduce_adamw, step=step,
                 gathers=R, h2d=W * gb * P, d2h=2 * P)
+
+
+def survey_bytes(wl: workloads.Workload, unit: int) -> int:
+    """The same unit step counted without the bf16 shadow write, every
+    operation separately: R gathers of 6P (4P when gathering the shadow),
+    the reduce-scatter's (W*g_b + 4)P and AdamW's 28P (30P with the shadow
+    gather, whose shadow write is then an input of the next gathers):
+    (44 + W*g_b)P, or (42 + W*g_b)P from the shadow."""
+    P, W = wl.unit_numel(unit), wl.world
+    gb = 4 if wl.grad_dtype == "f32" else 2
+    R = 2 if wl.reshard_after_forward else 1
+    if wl.gather_source == "shadow":
+        return (R * 4 + W * gb + 4 + 30) * P
+    return (R * 6 + W * gb + 4 + 28) * P
 
 
 L2_BYTES = 129e6   # GB300 L2 cache
@@ -244,13 +264,30 @@ def time_oracle_steps(wl: workloads.Workload, target_s: float, n_steps: int):
         orc.load(params)
         return sw, orc, grads
 
-    S = 1 << 20
-    sw, orc, grads = make(S)
-    dt = one(sw, orc, grads)
-    S = int(min(1 << 26, max(1 << 20, S * target_s / max(dt, 1e-6))))
+    S = calibrate_elements(wl, target_s, 1 << 26)
     sw, orc, grads = make(S)
     times = [one(sw, orc, grads) for _ in range(n_steps)]
     return times, S, counted_bytes(sw, 0)["step"]
+
+
+def calibrate_elements(wl: workloads.Workload, target_s: float, cap: int) -> int:
+    """Sample elements for which one oracle unit step takes about target_s on
+    one core (from a timed step on 2^20 elements), within [2^20, cap]."""
+    import numpy as np
+    from oracle import fsdp_oracle as O
+    S = 1 << 20
+    sw = oracle_sample_workload(wl, S)
+    params = [p.numpy() for p in workloads.param_tensors(sw, 0)]
+    grads = []
+    for r in range(sw.N):
+        g = workloads.grad_tensor(sw, 0, 0, r)
+        grads.append(g.numpy() if g.dtype == torch.float32 else g.view(torch.int16).numpy().view(np.uint16))
+    orc = O.UnitOracle(sw.shapes(0), sw.N, "flat", O.AdamWHyper(**workloads.hyper(sw)), sw.reshard_after_forward)
+    orc.load(params)
+    t0 = time.perf_counter()
+    orc.step(grads)
+    dt = time.perf_counter() - t0
+    return int(min(cap, max(1 << 20, S * target_s / max(dt, 1e-6))))
 
 
 def cpu_cores_info():
@@ -261,25 +298,144 @@ def cpu_cores_info():
     return aff
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                vendor = next((l.split(":", 1)[1].strip() for l in out.splitlines() if l.startswith("Vendor ID:")), "")
+                return f"{vendor} {line.split(':', 1)[1].strip()}".strip()
+    except Exception:
+        pass
+    try:
+        info = open("/proc/cpuinfo").read()
+        m = re.search(r"^model name\s*:\s*(.+)$", info, re.M)
+        if m:
+            return m.group(1).strip()
+        imp = re.search(r"^CPU implementer\s*:\s*(\S+)", info, re.M)
+        part = re.search(r"^CPU part\s*:\s*(\S+)", info, re.M)
+        if imp and part:
+            return f"CPU implementer {imp.group(1)} part {part.group(1)}"
+    except OSError:
+        pass
+    return "unknown"
+
+
+def _oracle_worker(wl, index, S, barrier, commands, results):
+    """One spawned worker of OracleTeam: builds its own FLAT sample unit of S
+    elements drawn like `wl` (its own seeds), then on every command runs one
+    unchanged oracle unit step, starting together with the other workers."""
+    import numpy as np
+    from oracle import fsdp_oracle as O
+    sw = oracle_sample_workload(wl, S).with_(name=f"{wl.name}_sample{S}_worker{index}")
+    params = [p.numpy() for p in workloads.param_tensors(sw, 0)]
+    grads = []
+    for r in range(sw.N):
+        g = workloads.grad_tensor(sw, 0, 0, r)
+        grads.append(g.numpy() if g.dtype == torch.float32 else g.view(torch.int16).numpy().view(np.uint16))
+    orc = O.UnitOracle(sw.shapes(0), sw.N, "flat", O.AdamWHyper(**workloads.hyper(sw)), sw.reshard_after_forward)
+    orc.load(params)
+    results.put(("ready", index, counted_bytes(sw, 0)["step"]))
+    while commands.get() is not None:
+        barrier.wait()
+        t0 = time.perf_counter()
+        orc.step(grads)
+        results.put(("done", index, time.perf_counter() - t0))
+
+
+class OracleTeam:
+    """n worker processes on the host cores (spawned, so that none inherits a
+    CUDA context), each holding a FLAT sample unit of `per_worker` elements
+    drawn like the workload; step() runs one oracle unit step on all of them at
+    once and returns the step's wall time (the slowest worker).  Every element
+    of the cycle is independent, so n disjoint samples stand for one sample n
+    times as large."""
+
+    def __init__(self, wl, n: int, per_worker: int):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.n = n
+        self.barrier = ctx.Barrier(n)
+        self.results = ctx.Queue()
+        self.commands = [ctx.Queue() for _ in range(n)]
+        self.procs = [ctx.Process(target=_oracle_worker, args=(wl, i, per_worker, self.barrier, self.commands[i],
+                                                               self.results), daemon=True) for i in range(n)]
+        for p in self.procs:
+            p.start()
+        ready = [self._get() for _ in range(n)]
+        self.step_bytes = sum(r[2] for r in ready)
+        self.elements = n * per_worker
+
+    def _get(self, limit_s: float = 600.0):
+        """The next worker message; raises if a worker died or nothing came."""
+        import queue
+        t0 = time.time()
+        while True:
+            try:
+                return self.results.get(timeout=1.0)
+            except queue.Empty:
+                dead = [p.exitcode for p in self.procs if p.exitcode not in (None, 0)]
+                if dead or time.time() - t0 > limit_s:
+                    self.close()
+                    raise RuntimeError(f"oracle worker failed (exit codes {dead})" if dead else
+                                       "oracle workers gave no answer")
+
+    def step(self) -> float:
+        for q in self.commands:
+            q.put(1)
+        return max(self._get()[2] for _ in range(self.n))
+
+    def close(self):
+        for p, q in zip(self.procs, self.commands):
+            if p.is_alive():
+                q.put(None)
+        for p in self.procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.terminate()
+
+
+def oracle_all_cores(wl, n_steps: int, per_worker: int, cores: int | None = None, warmup: int = 0):
+    """Per-step wall times of the oracle on every host core at once, after
+    `warmup` untimed steps.  Returns (times, elements per step, counted bytes
+    per step, workers)."""
+    n = cores or cpu_cores_info() or 1
+    team = OracleTeam(wl, n, per_worker)
+    try:
+        times = [team.step() for _ in range(warmup + n_steps)][warmup:]
+    finally:
+        team.close()
+    return times, team.elements, team.step_bytes, n
+
+
 # --------------------------------------------------------------------------- arms
 
 def run_reference(args, world, rank):
-    """The oracle as it stands, on the host cores: each step is one oracle unit
-    step on a bounded sample of the workload."""
+    """The oracle as it stands, on all the host's cores: each bench step is one
+    oracle unit step on every core at once, each core on its own bounded
+    sample of the workload (disjoint draws; the elements are independent).
+    A few one-core steps on one such sample are reported beside it."""
     if rank != 0:
         return
     wl = workloads.get(args.workload)
-    times, S, cb = time_oracle_steps(wl, target_s=args.ref_step_seconds, n_steps=args.warmup + args.steps)
+    per_worker = calibrate_elements(wl, args.ref_step_seconds, 1 << 24)
+    times, elems, cb, n = oracle_all_cores(wl, args.warmup + args.steps, per_worker)
     timed = times[args.warmup:]
     sec = sum(timed)
     value = cb * len(timed) / sec / 1e9
-    cpu = {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-           "sample": f"one FLAT unit of {S} elements drawn like {wl.name} (N={wl.N}, {wl.grad_dtype} grads), "
-                     f"one oracle step per bench step", "host_cores_available": cpu_cores_info()}
+    t1, S1, cb1 = time_oracle_steps(wl, target_s=args.ref_step_seconds, n_steps=2)
+    cpu = {"value": value, "unit": "GB/s", "cores": n, "kind": "oracle",
+           "sample": f"{n} worker processes, each one FLAT unit of {per_worker} elements drawn like {wl.name} "
+                     f"(N={wl.N}, {wl.grad_dtype} grads); one oracle unit step on all of them per bench step",
+           "elements_per_step": elems,
+           "host": {"cpu_model": cpu_model(), "cores_available": cpu_cores_info()},
+           "single_core": {"value": cb1 * len(t1) / sum(t1) / 1e9, "unit": "GB/s", "cores": 1,
+                           "sample": f"2 oracle unit steps on one FLAT unit of {S1} elements"}}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(timed),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": wl.name, "sample_elements": S},
+            "data": "synthetic", "config": {"workload": wl.name, "sample_elements": elems},
             "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -425,16 +581,25 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
-        times, S, ccb = time_oracle_steps(wl, target_s=args.cpu_seconds / 3, n_steps=3)
-        cpu = {"value": ccb * len(times) / sum(times) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"3 oracle unit steps on one FLAT unit of {S} elements drawn like {wl.name} "
-                         f"(N={wl.N}, {wl.grad_dtype} grads)", "host_cores_available": cpu_cores_info()}
+        cpu = cpu_baseline(args, wl)
 
     # FSDP_KSTATUS_* bits raised by any kernel during the run (0: none)
     kstatus = 0
     for u in units:
         kstatus |= u.kernel_status(stream)
         u.close()
+    del grads, out, units
+    torch.cuda.empty_cache()
+
+    # every other workload shape, timed the same way on the same GPU
+    configs = None
+    if args.configs and args.micro_batches == 1:
+        configs = {}
+        for name in CONFIG_WORKLOADS:
+            if name != wl.name:
+                configs[name] = run_config(args, workloads.get(name), dev, world)
+                kstatus |= configs[name].pop("kernel_status")
+    survey = sum(survey_bytes(wl, i) for i in range(wl.n_units))
     if rank != 0:
         return
     line = {
@@ -442,6 +607,9 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "pct_of_hbm_peak": 100.0 * value_rank / peak, "hbm_peak_gbs": peak, "hbm_peak_source": peak_kind,
+        "counted_bytes_per_step_survey": survey,
+        "value_survey": world * survey * args.steps / (ms_max * 1e-3) / 1e9,
+        "pct_of_hbm_peak_survey": 100.0 * survey * args.steps / (ms * 1e-3) / 1e9 / peak,
         "config": {"workload": wl.name, "units": wl.n_units, "params_per_unit": [u_ for u_ in
                    (wl.unit_numel(i) for i in range(wl.n_units))], "virtual_ranks": wl.N,
                    "layout": wl.layout, "grad_dtype": wl.grad_dtype,
@@ -453,9 +621,120 @@ def run_ours(args, world, rank, local):
                    "l2": l2_statement(wl), "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "graph": graph, "unprofiled": unprofiled, "fastest_variant": fastest, "kernel_status": kstatus,
-        "clocks": clk.result,
+        "clocks": clk.result, "configs": configs,
     }
     print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(args, wl) -> dict:
+    """The oracle on the host cores: all cores at once (the reported value)
+    and one core, each over 3 unit steps of bounded samples of the workload."""
+    times, S, ccb = time_oracle_steps(wl, target_s=args.cpu_seconds / 6, n_steps=3)
+    single = {"value": ccb * len(times) / sum(times) / 1e9, "unit": "GB/s", "cores": 1,
+              "sample": f"3 oracle unit steps on one FLAT unit of {S} elements"}
+    per_worker = min(S, 1 << 24)
+    at, elems, acb, n = oracle_all_cores(wl, 3, per_worker, warmup=1)
+    return {"value": acb * len(at) / sum(at) / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"3 oracle unit steps on {n} worker processes at once, each one FLAT unit of "
+                      f"{per_worker} elements drawn like {wl.name} (N={wl.N}, {wl.grad_dtype} grads)",
+            "elements_per_step": elems,
+            "host": {"cpu_model": cpu_model(), "cores_available": cpu_cores_info()},
+            "single_core": single}
+
+
+# the workloads timed besides the headline one, each on its own
+CONFIG_WORKLOADS = ("tiny_flat", "gpt2_small_flat", "gpt2_large_dim0", "ragged_flat_n7", "ragged_dim0_n7",
+                    "ragged_flat_n64", "ragged_dim0_n64", "mingpt175b_flat")
+
+
+def run_config(args, wl: workloads.Workload, dev, world) -> dict:
+    """One workload's model step (fsdp_step on every unit) timed with CUDA
+    events around K steps on the launch stream; each kernel's time per launch
+    from K back-to-back rounds of that kernel alone over every unit; and the
+    step again with the per-launch profiler's event pairs (which serialise the
+    launches: `profiled_ms_per_step`).  K is chosen so the timed region lasts
+    about 0.2 s (at least 10 steps)."""
+    from fully_sharded_unit_gb300 import binding as B
+    hp = workloads.hyper(wl)
+    units = []
+    for i in range(wl.n_units):
+        u = B.Unit(wl.shapes(i), wl.layout, wl.N, wl.grad_dtype, wl.reshard_after_forward, replicas=wl.replicas,
+                   reduce_dtype=wl.reduce_dtype, gather_source=wl.gather_source,
+                   fuse_reduce_adamw=wl.fuse_reduce_adamw)
+        u.load(workloads.param_tensors(wl, i, dev))
+        units.append(u)
+    P_max = max(u.numel for u in units)
+    grads = [torch.empty(P_max, dtype=wl.torch_grad_dtype(), device=dev) for _ in range(wl.world)]
+    for r in range(wl.world):
+        workloads.grad_tensor(wl, 0, 0, r, dev, out=grads[r][:units[0].numel])
+    out = torch.empty(P_max, dtype=torch.int16, device=dev)
+    stream = torch.cuda.current_stream()
+    views = [grads if u.numel == P_max else [g[:u.numel] for g in grads] for u in units]
+
+    def step():
+        for u, g in zip(units, views):
+            u.step(g, out, hp, stream)
+
+    def timed(k):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dist_barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(k):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return dist_max(ev0.elapsed_time(ev1), world, dev)
+
+    est = timed(max(3, args.warmup)) / max(3, args.warmup)
+    K = int(min(1000, max(10, round(200.0 / max(est, 1e-3)))))
+    ms = timed(K) / K
+    cb = [counted_bytes(wl, i) for i in range(wl.n_units)]
+    # each kernel alone, launched back to back over every unit K times (no
+    # events between launches, so launches overlap as in the step); AdamW
+    # advances the units' state, which changes nothing in its bytes or time
+    # (the C entry points with their arguments marshalled once, so that the
+    # host's launch rate does not bound the small units)
+    import ctypes
+    lib, sh = B.lib(), stream.cuda_stream
+    hp_c = B._hp(hp)
+    ptrs = {id(g): B._ptrs(g) for g in views}
+    calls = {"gather": lambda u, g: lib.fsdp_allgather(u.handle, out.data_ptr(), sh),
+             "reduce_scatter": lambda u, g: lib.fsdp_reduce_scatter(u.handle, ptrs[id(g)], sh),
+             "adamw": lambda u, g: lib.fsdp_adamw_step(u.handle, ctypes.byref(hp_c), sh)}
+    kernels = {}
+    for k, call in calls.items():
+        def one_kernel(k_steps, call=call):
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            ev0.record(stream)
+            for _ in range(k_steps):
+                for u, g in zip(units, views):
+                    rc = call(u, g)
+                    assert rc == B.FSDP_OK, B.fsdp_last_error()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            return ev0.elapsed_time(ev1)
+        one_kernel(2)
+        kms = one_kernel(K) / (K * wl.n_units)
+        kernels[k] = {"ms_per_launch": kms, "gbs": sum(c[k] for c in cb) / wl.n_units / (kms * 1e-3) / 1e9}
+    for u in units:
+        B.fsdp_profile_reset(u.handle)
+        B.fsdp_profile_enable(u.handle, True)
+    pms = timed(K) / K
+    kstatus = 0
+    for u in units:
+        kstatus |= u.kernel_status(stream)
+        u.close()
+    step_bytes = sum(c["step"] for c in cb)
+    survey = sum(survey_bytes(wl, i) for i in range(wl.n_units))
+    peak, _ = measured_peak()
+    return {"units": wl.n_units, "params_per_unit": wl.unit_numel(0), "virtual_ranks": wl.N, "layout": wl.layout,
+            "grad_dtype": wl.grad_dtype, "steps": K, "ms_per_step": ms, "ms_per_unit_step": ms / wl.n_units,
+            "counted_bytes_per_step": step_bytes, "value": world * step_bytes / (ms * 1e-3) / 1e9,
+            "counted_bytes_per_step_survey": survey, "value_survey": world * survey / (ms * 1e-3) / 1e9,
+            "pct_of_hbm_peak_survey": 100.0 * survey / (ms * 1e-3) / 1e9 / peak, "unit": "GB/s",
+            "profiled_ms_per_step": pms, "kernels": kernels, "l2": l2_statement(wl), "kernel_status": kstatus}
 
 
 def run_variant(args, units, step, stream, hp, world, dev, vwl):
@@ -644,6 +923,8 @@ def main(argv=None):
                          "(device-side AdamW step counter)")
     ap.add_argument("--fuse", choices=["on", "off"], default=None,
                     help="override whether fsdp_step fuses reduce-scatter and AdamW")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip timing the other workloads (the 'configs' object)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
