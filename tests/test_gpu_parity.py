@@ -68,6 +68,23 @@ def test_edge_shapes(shapes, N, layout):
     H.run_full(_custom(shapes, N, layout, grad_dtype="bf16", name="custom_bf16"), use_step=True)
 
 
+@pytest.mark.parametrize("layout,N,R,grad_dtype,kw", [
+    ("flat", 1024, 1, "f32", {}),                                   # the most ranks a unit takes
+    ("dim0", 1024, 1, "bf16", {}),                                  # fewer dim-0 rows than ranks
+    ("flat", 1024, 1, "bf16", {"reduce_dtype": "bf16"}),
+    ("flat", 1024, 1, "f32", {"fuse_reduce_adamw": True}),          # register-staged fused kernel
+    ("flat", 64, 16, "f32", {}),                                    # hybrid: W = 1024 gradients
+    ("dim0", 128, 8, "bf16", {"fuse_reduce_adamw": True}),          # hybrid fused, W = 1024
+])
+def test_maximum_rank_count(layout, N, R, grad_dtype, kw):
+    """W = N * replicas = 1024, the library's maximum: 1024 gradient pointers
+    per launch, ranks whose shards are a few elements or empty."""
+    wl = _custom([(300, 257), (1000,), (7, 3)], N, layout, grad_dtype=grad_dtype, steps=2,
+                 name=f"max_ranks_{grad_dtype}").with_(replicas=R, **kw)
+    cmp = H.run_full(wl, use_step=True)
+    assert cmp.total_diff == 0
+
+
 def test_no_reshard_after_forward_gathers_once():
     H.run_full(_custom([(77, 5)], 4, "flat", raf=False), use_step=True)
     H.run_full(_custom([(77, 5)], 4, "dim0", raf=False))
