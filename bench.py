@@ -798,7 +798,15 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world)
       zero_copy -- the reduce-scatter reads the pinned host gradients directly
                    over the host link (device addresses from
                    fsdp_host_device_pointer);
-      copy      -- cudaMemcpyAsync of each gradient host->device first.
+      copy      -- cudaMemcpyAsync of each gradient host->device first, on
+                   the compute stream;
+      pipelined -- the same copies on a stream of their own, into two device
+                   sets of gradients used by alternate units, so that a unit's
+                   gradients cross the host link while the unit before it
+                   computes (the first unit of the next step while this step's
+                   last unit computes); the reduce-scatter waits for its unit's
+                   copies.  Every timed step's copies start after the timed
+                   region opens.
     The unit step is issued as its calls (gather, gather again, reduce-scatter,
     AdamW: the work of fsdp_step) so that the gathered parameters, final after
     the first gather, are copied to the host on a second stream while the rest
@@ -829,19 +837,47 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world)
     host_out = [torch.empty(P_max, dtype=torch.int16, pin_memory=True) for _ in units]
     outs = [(out, torch.empty_like(out)), (torch.empty_like(out), torch.empty_like(out))]
     copy_stream = torch.cuda.Stream(device=dev)
-    if args.e2e_mode == "zero_copy":
+    h2d_stream = torch.cuda.Stream(device=dev)
+    mode = args.e2e_mode
+    if mode == "zero_copy":
         unit_grads = [[B.fsdp_host_device_pointer(h[:u.numel]) for h in host_grads] for u in units]
+    elif mode == "pipelined":
+        # two device sets of the gradients, used by alternate units: a unit's
+        # gradients are copied in while the unit before it computes
+        sets = [grads] + ([[torch.empty_like(g) for g in grads]] if len(units) > 1 else [])
+        unit_grads = [[g[:u.numel] for g in sets[i % len(sets)]] for i, u in enumerate(units)]
     else:
         unit_grads = [[g[:u.numel] for g in grads] for u in units]
     free = [None, None]      # events: last D2H copy out of outs[k][0] finished
+    consumed = [None, None]  # events: the reduce-scatter that read gradient set k has finished
+    pending = {}             # unit -> event: its gradients are on the device (pipelined)
 
-    def step():
+    def issue_copy(i):
+        """Unit i's gradients host->device on the copy stream, into its set,
+        once the reduce-scatter that last read that set has finished."""
+        u, k = units[i], i % 2
+        if consumed[k] is not None:
+            h2d_stream.wait_event(consumed[k])
+        with torch.cuda.stream(h2d_stream):
+            for h, g in zip(host_grads, unit_grads[i]):
+                g.copy_(h[:u.numel], non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(h2d_stream)
+        pending[i] = ev
+
+    def step(prefetch=False):
+        """One e2e step; with `prefetch` (pipelined) the next step's first
+        unit's gradients are queued for copying at the end."""
         done = []
+        if mode == "pipelined" and 0 not in pending:
+            issue_copy(0)
         for i, u in enumerate(units):
+            if mode == "pipelined" and i + 1 < len(units):
+                issue_copy(i + 1)           # copied while this unit computes
             first, second = outs[i % 2]
             if free[i % 2] is not None:
                 stream.wait_event(free[i % 2])
-            if args.e2e_mode == "copy":
+            if mode == "copy":
                 for h, g in zip(host_grads, grads):
                     g[:u.numel].copy_(h[:u.numel], non_blocking=True)
             u.allgather(first[:u.numel], stream)
@@ -856,10 +892,18 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world)
             done.append(ev)
             if wl.reshard_after_forward:
                 u.allgather(second[:u.numel], stream)
+            if mode == "pipelined":
+                stream.wait_event(pending.pop(i))
             u.reduce_scatter(unit_grads[i], stream)
+            if mode == "pipelined":
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                consumed[i % 2] = ev
             u.adamw_step(hp, stream)
         for ev in done:
             stream.wait_event(ev)
+        if mode == "pipelined" and prefetch:
+            issue_copy(0)
 
     step()
     torch.cuda.synchronize()
@@ -867,8 +911,9 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world)
     dist_barrier(world)
     torch.cuda.synchronize()
     ev0.record(stream)
-    for _ in range(args.e2e_steps):
-        step()
+    h2d_stream.wait_event(ev0)     # every timed step's copies start inside the timed region
+    for j in range(args.e2e_steps):
+        step(prefetch=j + 1 < args.e2e_steps)
     ev1.record(stream)
     torch.cuda.synchronize()
     dist_barrier(world)
@@ -876,9 +921,11 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world)
     h2d = sum(c["h2d"] for c in cb)
     d2h = sum(c["d2h"] for c in cb)
     del host_grads, host_out, unit_grads, outs
+    if mode == "pipelined":
+        del sets
     return {"value": world * step_bytes * args.e2e_steps / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "ms_per_step": ms / args.e2e_steps, "mode": args.e2e_mode, "inputs": inputs}
+            "ms_per_step": ms / args.e2e_steps, "mode": mode, "inputs": inputs}
 
 
 def host_mem_available():
@@ -901,7 +948,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mingpt175b_flat", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--e2e-mode", choices=["zero_copy", "copy"], default="zero_copy")
+    ap.add_argument("--e2e-mode", choices=["pipelined", "zero_copy", "copy"], default="pipelined",
+                    help="pipelined: gradients copied host->device on their own stream into two "
+                         "alternating device sets while the previous unit computes; zero_copy: the "
+                         "reduce-scatter reads pinned host memory directly; copy: copies on the "
+                         "compute stream")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
