@@ -12,12 +12,13 @@ Metric: counted HBM bytes per step / step time (GB/s).  Counted bytes per
 unit step, every required read and write once:
     gather      R x (4P read fp32 master + 2P write bf16)          R = 2
     reduce-sc.  N*g_b*P read (N gradients) + 4P write (fp32 shards)
-    AdamW       16P read (p, g, m, v) + 12P write (p, m, v) + 2P (bf16 shadow)
+    AdamW       16P read (p, g, m, v) + 12P write (p, m, v)
+                (+ 2P for the bf16 shadow when the unit gathers from it)
 
-The line also carries the same step counted the survey's way, without the
-bf16 shadow write ((44 + N*g_b)P per unit, "value_survey"), the oracle's
-throughput on the host cores (all cores and one), and a "configs" object with
-every other workload's model step timed the same way.
+The line also carries the same step counted the survey's way ((44 + N*g_b)P
+per unit, "value_survey"; the same count as above unless the fused kernel
+runs), the oracle's throughput on the host cores (all cores and one), and a
+"configs" object with every other workload's model step timed the same way.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload NAME] [--e2e-steps E] [--no-e2e] [--no-cpu-baseline]
@@ -58,22 +59,24 @@ def counted_bytes(wl: workloads.Workload, unit: int) -> dict:
     P, W = wl.unit_numel(unit), wl.world
     gb = 4 if wl.grad_dtype == "f32" else 2
     R = 2 if wl.reshard_after_forward else 1
-    gather = (2 if wl.gather_source == "shadow" else 4) * P + 2 * P
+    shadow = wl.gather_source == "shadow"   # AdamW stores the bf16 shadow only when it is gathered from
+    gather = (2 if shadow else 4) * P + 2 * P
     rs = (W * gb + 4) * P
-    adamw = 30 * P
+    adamw = (30 if shadow else 28) * P
     # fused: the gradient shard is written (4P) but not read back
-    reduce_adamw = (W * gb + 4 + 12 + 12 + 2) * P
+    reduce_adamw = (W * gb + 4 + 12 + 12 + (2 if shadow else 0)) * P
     step = R * gather + (reduce_adamw if wl.fuse_reduce_adamw else rs + adamw)
     return dict(gather=gather, reduce_scatter=rs, adamw=adamw, reduce_adamw=reduce_adamw, step=step,
                 gathers=R, h2d=W * gb * P, d2h=2 * P)
 
 
 def survey_bytes(wl: workloads.Workload, unit: int) -> int:
-    """The same unit step counted without the bf16 shadow write, every
-    operation separately: R gathers of 6P (4P when gathering the shadow),
-    the reduce-scatter's (W*g_b + 4)P and AdamW's 28P (30P with the shadow
-    gather, whose shadow write is then an input of the next gathers):
-    (44 + W*g_b)P, or (42 + W*g_b)P from the shadow."""
+    """The unit step counted the survey's way, every operation separately:
+    R gathers of 6P (4P when gathering the shadow), the reduce-scatter's
+    (W*g_b + 4)P and AdamW's 28P (30P with the shadow gather, whose shadow
+    write is then an input of the next gathers): (44 + W*g_b)P, or
+    (42 + W*g_b)P from the shadow.  It differs from counted_bytes only for
+    the fused kernel, which does not read the gradient shard back."""
     P, W = wl.unit_numel(unit), wl.world
     gb = 4 if wl.grad_dtype == "f32" else 2
     R = 2 if wl.reshard_after_forward else 1

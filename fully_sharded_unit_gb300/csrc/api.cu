@@ -5,6 +5,11 @@
 // [arena_base[k], arena_base[k] + arena_len[k]) of each.  Pads are zero from
 // creation and stay zero: the gather and reduce-scatter never touch them and
 // AdamW maps (p, g, m, v) = 0 to 0.
+//
+// The bf16 shadow equals RNE(master) whenever anything reads it.  AdamW
+// stores it only when the unit gathers from it; otherwise the unit marks it
+// stale, and the next read (a gather from it, a state export) first runs one
+// cast pass over the slab.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -106,6 +111,7 @@ struct fsdp_unit {
     fsdp::ParamSrc* param_src = nullptr;
     int64_t t = 0;
     bool loaded = false;
+    mutable bool shadow_valid = true;   // the shadow slab holds RNE(master)
     bool profiling = false;
     std::vector<ProfRecord> prof;
 };
@@ -285,8 +291,18 @@ fsdp::AdamWConsts adamw_consts(const fsdp_adamw_hp* hp, int64_t t) {
     return c;
 }
 
+// Recompute the whole shadow slab from the master if AdamW left it stale.
+int ensure_shadow(const fsdp_unit* u, cudaStream_t st) {
+    if (u->shadow_valid) return FSDP_OK;
+    cudaError_t e = fsdp::launch_cast_range(u->master, u->shadow, 0, u->plan.slab_len, st);
+    if (e != cudaSuccess) return cuda_fail(e, "shadow refresh");
+    u->shadow_valid = true;
+    return FSDP_OK;
+}
+
 fsdp::StepSource step_source(const fsdp_unit* u, const fsdp_adamw_hp* hp) {
     fsdp::StepSource s{};
+    s.write_shadow = u->gather_source == FSDP_GATHER_FROM_SHADOW ? 1 : 0;
     if (u->device_steps) {
         s.table = u->step_table;
         s.counter = u->step_counter;
@@ -306,6 +322,10 @@ int advance_device_step(fsdp_unit* u, cudaStream_t st) {
 }
 
 int enqueue_gather(fsdp_unit* u, uint16_t* out, cudaStream_t st) {
+    if (u->gather_source == FSDP_GATHER_FROM_SHADOW) {
+        int rc = ensure_shadow(u, st);
+        if (rc) return rc;
+    }
     return profiled_launch(u, FSDP_KERNEL_GATHER, st, "gather launch", [&] {
         if (u->gather_source == FSDP_GATHER_FROM_SHADOW)
             return fsdp::launch_gather_shadow(u->tiles, u->ntiles, u->shadow, out, st);
@@ -358,10 +378,15 @@ int enqueue_reduce_adamw(fsdp_unit* u, const void* const* grads, int narrow, con
     a.narrow = narrow;
     wait_args(u, &a);
     const fsdp::StepSource c = step_source(u, hp);
-    int rc = profiled_launch(u, FSDP_KERNEL_REDUCE_ADAMW, st, "fused reduce-scatter + AdamW launch", [&] {
-        return fsdp::launch_reduce_adamw(u->tiles, u->ntiles, grads, u->grad_dtype, a, u->grad, u->master,
-                                         u->m, u->v, u->shadow, c, u->kstatus, st);
-    });
+    // a step that is skipped on the device (used-up step table) leaves the
+    // shadow as it was, so a stale one is refreshed before a storing launch
+    int rc = c.write_shadow ? ensure_shadow(u, st) : FSDP_OK;
+    if (rc == FSDP_OK)
+        rc = profiled_launch(u, FSDP_KERNEL_REDUCE_ADAMW, st, "fused reduce-scatter + AdamW launch", [&] {
+            return fsdp::launch_reduce_adamw(u->tiles, u->ntiles, grads, u->grad_dtype, a, u->grad, u->master,
+                                             u->m, u->v, u->shadow, c, u->kstatus, st);
+        });
+    if (rc == FSDP_OK) u->shadow_valid = c.write_shadow != 0;
     if (rc == FSDP_OK) rc = advance_device_step(u, st);
     if (rc == FSDP_OK) u->t += 1;
     return rc;
@@ -369,9 +394,12 @@ int enqueue_reduce_adamw(fsdp_unit* u, const void* const* grads, int narrow, con
 
 int enqueue_adamw(fsdp_unit* u, const fsdp_adamw_hp* hp, cudaStream_t st) {
     const fsdp::StepSource c = step_source(u, hp);
-    int rc = profiled_launch(u, FSDP_KERNEL_ADAMW, st, "AdamW launch", [&] {
-        return fsdp::launch_adamw(u->plan.slab_len / 8, u->master, u->grad, u->m, u->v, u->shadow, c, st);
-    });
+    int rc = c.write_shadow ? ensure_shadow(u, st) : FSDP_OK;
+    if (rc == FSDP_OK)
+        rc = profiled_launch(u, FSDP_KERNEL_ADAMW, st, "AdamW launch", [&] {
+            return fsdp::launch_adamw(u->plan.slab_len / 8, u->master, u->grad, u->m, u->v, u->shadow, c, st);
+        });
+    if (rc == FSDP_OK) u->shadow_valid = c.write_shadow != 0;
     if (rc == FSDP_OK) rc = advance_device_step(u, st);
     if (rc == FSDP_OK) u->t += 1;
     return rc;
@@ -615,6 +643,7 @@ int fsdp_load_params(fsdp_unit* u, const float* const* params, void* stream) {
     u->device_steps = false;
     u->loaded = true;
     u->needs_reload = false;
+    u->shadow_valid = true;   // shard-in writes RNE(master)
     return FSDP_OK;
 }
 
@@ -704,6 +733,10 @@ static int copy_state(const fsdp_unit* u, int which, int rank, void* ext, bool t
     DeviceGuard dg(u->device);
     if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (which == FSDP_STATE_SHADOW) {   // read: refresh a stale shadow; write: start from a fresh one
+        rc = ensure_shadow(u, st);
+        if (rc) return rc;
+    }
     const int64_t abase = u->plan.arena_base[rank];
     for (int64_t i = u->plan.rank_first_seg[rank]; i < u->plan.rank_first_seg[rank + 1]; ++i) {
         const fsdp_segment& s = u->plan.segs[i];
@@ -741,6 +774,10 @@ int fsdp_read_global(const fsdp_unit* u, int which, int64_t begin, int64_t count
     DeviceGuard dg(u->device);
     if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (which == FSDP_STATE_SHADOW) {
+        rc = ensure_shadow(u, st);
+        if (rc) return rc;
+    }
     const int64_t end = begin + count;
     for (const fsdp_segment& s : u->plan.segs) {
         const int64_t a = s.global_off > begin ? s.global_off : begin;
@@ -767,6 +804,10 @@ int fsdp_read_arena(const fsdp_unit* u, int which, int rank, void* dst, int64_t*
     if (dst == nullptr) return FSDP_OK;   // size query
     DeviceGuard dg(u->device);
     if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
+    if (which == FSDP_STATE_SHADOW) {
+        rc = ensure_shadow(u, static_cast<cudaStream_t>(stream));
+        if (rc) return rc;
+    }
     cudaError_t e = cudaMemcpyAsync(dst, base + static_cast<size_t>(u->plan.arena_base[rank]) * esz,
                                     static_cast<size_t>(n) * esz, cudaMemcpyDefault,
                                     static_cast<cudaStream_t>(stream));

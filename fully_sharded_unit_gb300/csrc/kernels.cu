@@ -673,7 +673,7 @@ __global__ void __launch_bounds__(kBlock) adamw_kernel(int64_t n8, float* __rest
         st8(p + 8 * i, P);
         st8(m + 8 * i, M);
         st8(v + 8 * i, V);
-        st8bf(shadow + 8 * i, pack8(P));
+        if (src.write_shadow) st8bf(shadow + 8 * i, pack8(P));
     }
 }
 
@@ -735,7 +735,7 @@ __global__ void __launch_bounds__(kBlock, sizeof(GT) == 2 ? 3 : 2) reduce_adamw_
             p[s] = pp;
             m[s] = mm;
             v[s] = vv;
-            shadow[s] = to_bf16(pp);
+            if (src.write_shadow) shadow[s] = to_bf16(pp);
         }
 #pragma unroll 1
         for (int vi = tid; vi < sp.nvec; vi += kBlock) {
@@ -751,7 +751,7 @@ __global__ void __launch_bounds__(kBlock, sizeof(GT) == 2 ? 3 : 2) reduce_adamw_
             st8(p + s, P);
             st8(m + s, M);
             st8(v + s, V);
-            st8bf(shadow + s, pack8(P));
+            if (src.write_shadow) st8bf(shadow + s, pack8(P));
         }
     }
 }
@@ -1020,7 +1020,7 @@ __global__ void __launch_bounds__(kBlock) reduce_adamw_bulk_kernel(const Tile* _
             p[s] = pp;
             m[s] = mm;
             v[s] = vv;
-            shadow[s] = to_bf16(pp);
+            if (src.write_shadow) shadow[s] = to_bf16(pp);
         }
         const int64_t nch = (b.n + CH - 1) / CH;
         for (int64_t ch = 0; ch < nch; ++ch) {
@@ -1047,7 +1047,8 @@ __global__ void __launch_bounds__(kBlock) reduce_adamw_bulk_kernel(const Tile* _
                 *reinterpret_cast<float4*>(p + so) = P;
                 *reinterpret_cast<float4*>(m + so) = M;
                 *reinterpret_cast<float4*>(v + so) = V;
-                *reinterpret_cast<uint2*>(shadow + so) = make_uint2(pack_bf16x2(P.x, P.y), pack_bf16x2(P.z, P.w));
+                if (src.write_shadow)
+                    *reinterpret_cast<uint2*>(shadow + so) = make_uint2(pack_bf16x2(P.x, P.y), pack_bf16x2(P.z, P.w));
             }
             ++consumed;
             ok = __syncthreads_and(got) != 0;

@@ -28,6 +28,7 @@ struct StepSource {
     const int64_t* counter;     // device: steps taken since the table was made
     int64_t count;              // table length
     int32_t* status;            // device: set to 1 when a step finds the table used up
+    int write_shadow;           // 1: also store the bf16 shadow RNE(p) of every updated element
 };
 
 struct ParamSrc {

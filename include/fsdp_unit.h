@@ -82,7 +82,7 @@ extern "C" {
 
 /* where the all-gather reads from */
 #define FSDP_GATHER_FROM_MASTER 0  /* fp32 master shard, cast to bf16 while gathering */
-#define FSDP_GATHER_FROM_SHADOW 1  /* bf16 shadow shard (always RNE(master)), copied  */
+#define FSDP_GATHER_FROM_SHADOW 1  /* bf16 shadow shard (RNE(master) when read), copied */
 
 /* per-rank state a unit owns */
 #define FSDP_STATE_PARAM      0  /* fp32 sharded master parameters           */
@@ -235,8 +235,9 @@ FSDP_API int fsdp_load_params(fsdp_unit* unit, const float* const* params_dev, v
  * one buffer, since every virtual rank's result is the same.  Rounding is
  * IEEE round-to-nearest-even; NaN stays NaN.  With gather_source
  * FSDP_GATHER_FROM_SHADOW the same bytes are copied from the bf16 shadow
- * shards (which always hold RNE(master)): the gather then moves bf16, as when
- * the collective runs in the low precision ([FSDP] 4.4). */
+ * shards (which hold RNE(master) whenever they are read; see fsdp_adamw_step):
+ * the gather then moves bf16, as when the collective runs in the low precision
+ * ([FSDP] 4.4). */
 FSDP_API int fsdp_allgather(fsdp_unit* unit, uint16_t* out_bf16_dev, void* stream);
 
 /* Reduce-scatter ([ARCH] backward step 3: sum the ranks' gradients and give
@@ -275,6 +276,12 @@ FSDP_API int fsdp_zero_grad(fsdp_unit* unit, void* stream);
  *     p = p - fp32(lr/(1-beta1^t)) * (m / (sqrt(v / fp32(1-beta2^t)) + fp32(eps)))
  *     shadow = RNE_bf16(p)
  * The scalar constants are formed in double on the host and rounded once.
+ * The bf16 shadow holds RNE_bf16(p) whenever it is read: the update stores it
+ * when the unit gathers from the shadow (gather_source FSDP_GATHER_FROM_SHADOW);
+ * otherwise the store is skipped (2 bytes per element less) and the next read
+ * of the shadow (a gather from it, fsdp_get_state, fsdp_read_global or
+ * fsdp_read_arena of FSDP_STATE_SHADOW) first recomputes it on that call's
+ * stream.
  * The step count advances when the launch is enqueued; if a kernel of this
  * unit later reports a status bit (fsdp_kernel_status), the count no longer
  * matches the state and the unit must be reloaded. */
@@ -294,9 +301,10 @@ FSDP_API int fsdp_step(fsdp_unit* unit, const void* const* grads_dev, uint16_t* 
 
 /* Change how fsdp_step runs on an existing unit: gather_source
  * (FSDP_GATHER_FROM_MASTER or _FROM_SHADOW) and fuse_reduce_adamw, as in
- * fsdp_unit_config.  Results do not depend on either choice (the shadow always
- * holds RNE(master), and the fused kernel performs the same operations), only
- * the bytes moved do.  Takes effect for calls enqueued afterwards. */
+ * fsdp_unit_config.  Results do not depend on either choice (the shadow holds
+ * RNE(master) whenever it is read, and the fused kernel performs the same
+ * operations), only the bytes moved do.  Takes effect for calls enqueued
+ * afterwards. */
 FSDP_API int fsdp_unit_set_step_options(fsdp_unit* unit, int gather_source, int fuse_reduce_adamw);
 
 /* ---- reduce-scatter without device allocation ------------------------------ */

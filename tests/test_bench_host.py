@@ -33,13 +33,16 @@ def test_recorded_traffic_file_parses_and_unknown_keys_give_none():
 
 def test_counted_bytes_per_launch():
     """Algorithmic bytes per element: gather 6 (4 from the shadow), reduce-scatter
-    W*g_b + 4, AdamW 30, fused W*g_b + 30; a unit step sums them."""
+    W*g_b + 4, AdamW 28 (30 when it also stores the shadow the gathers read),
+    fused W*g_b + 28 (+2); a unit step sums them, and with the separate kernels
+    it equals the survey's (44 + W*g_b) count."""
     wl = workloads.get("mingpt175b_flat")
     P = wl.unit_numel(0)
     c = bench.counted_bytes(wl, 0)
-    assert (c["gather"], c["reduce_scatter"], c["adamw"], c["reduce_adamw"]) == (6 * P, 20 * P, 30 * P, 46 * P)
-    assert c["step"] == 2 * 6 * P + 20 * P + 30 * P
+    assert (c["gather"], c["reduce_scatter"], c["adamw"], c["reduce_adamw"]) == (6 * P, 20 * P, 28 * P, 44 * P)
+    assert c["step"] == 2 * 6 * P + 20 * P + 28 * P == bench.survey_bytes(wl, 0) == (44 + 16) * P
     f = bench.counted_bytes(wl.with_(fuse_reduce_adamw=True, gather_source="shadow"), 0)
-    assert f["gather"] == 4 * P and f["step"] == 2 * 4 * P + 46 * P
+    assert f["gather"] == 4 * P and f["adamw"] == 30 * P and f["step"] == 2 * 4 * P + 46 * P
+    assert bench.survey_bytes(wl.with_(gather_source="shadow"), 0) == (42 + 16) * P
     h = bench.counted_bytes(wl.with_(replicas=2), 0)
     assert h["reduce_scatter"] == (16 * 2 + 4) * P
