@@ -46,3 +46,14 @@ def test_counted_bytes_per_launch():
     assert bench.survey_bytes(wl.with_(gather_source="shadow"), 0) == (42 + 16) * P
     h = bench.counted_bytes(wl.with_(replicas=2), 0)
     assert h["reduce_scatter"] == (16 * 2 + 4) * P
+
+
+def test_oracle_on_several_cores_times_every_worker():
+    """The all-core CPU baseline: two spawned workers, each with its own
+    sample, run one oracle unit step at once per bench step."""
+    wl = workloads.get("mingpt175b_flat")
+    times, elements, step_bytes, workers = bench.oracle_all_cores(wl, 2, 1 << 20, cores=2, warmup=1)
+    assert workers == 2 and elements == 2 << 20 and len(times) == 2 and min(times) > 0
+    sample = bench.oracle_sample_workload(wl, 1 << 20)
+    assert step_bytes == 2 * bench.counted_bytes(sample, 0)["step"]
+    assert bench.cpu_model()
