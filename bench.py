@@ -446,6 +446,8 @@ def run_reference(args, world, rank):
 
 def selected_workload(args) -> workloads.Workload:
     wl = workloads.get(args.workload)
+    if args.units is not None:          # profiling a few units of a many-unit model
+        wl = wl.with_(units=wl.units[:args.units])
     over = {k: v for k, v in (("gather_source", args.gather_source), ("layout", args.layout),
                               ("reduce_dtype", args.reduce_dtype),
                               ("fuse_reduce_adamw", None if args.fuse is None else args.fuse == "on"),
@@ -988,6 +990,8 @@ def main(argv=None):
                          "(device-side AdamW step counter)")
     ap.add_argument("--fuse", choices=["on", "off"], default=None,
                     help="override whether fsdp_step fuses reduce-scatter and AdamW")
+    ap.add_argument("--units", type=int, default=None,
+                    help="time only the first K units of the workload (for small profiling captures)")
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="skip timing the other workloads (the 'configs' object)")
     args = ap.parse_args(argv)
