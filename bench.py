@@ -15,10 +15,11 @@ unit step, every required read and write once:
     AdamW       16P read (p, g, m, v) + 12P write (p, m, v)
                 (+ 2P for the bf16 shadow when the unit gathers from it)
 
-The line also carries the same step counted the survey's way ((44 + N*g_b)P
-per unit, "value_survey"; the same count as above unless the fused kernel
-runs), the oracle's throughput on the host cores (all cores and one), and a
-"configs" object with every other workload's model step timed the same way.
+The line also carries the same step counted with every operation separate
+((44 + N*g_b)P per unit, "value_survey"; the same count as above unless the
+fused kernel runs), the oracle's throughput on the host cores (all cores and
+one), and a "configs" object with every other workload's model step timed the
+same way.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload NAME] [--e2e-steps E] [--no-e2e] [--no-cpu-baseline]
@@ -71,7 +72,7 @@ def counted_bytes(wl: workloads.Workload, unit: int) -> dict:
 
 
 def survey_bytes(wl: workloads.Workload, unit: int) -> int:
-    """The unit step counted the survey's way, every operation separately:
+    """The unit step counted with every operation separate:
     R gathers of 6P (4P when gathering the shadow), the reduce-scatter's
     (W*g_b + 4)P and AdamW's 28P (30P with the shadow gather, whose shadow
     write is then an input of the next gathers): (44 + W*g_b)P, or

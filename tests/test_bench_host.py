@@ -35,7 +35,7 @@ def test_counted_bytes_per_launch():
     """Algorithmic bytes per element: gather 6 (4 from the shadow), reduce-scatter
     W*g_b + 4, AdamW 28 (30 when it also stores the shadow the gathers read),
     fused W*g_b + 28 (+2); a unit step sums them, and with the separate kernels
-    it equals the survey's (44 + W*g_b) count."""
+    it equals the every-operation-separate (44 + W*g_b) count."""
     wl = workloads.get("mingpt175b_flat")
     P = wl.unit_numel(0)
     c = bench.counted_bytes(wl, 0)
