@@ -321,15 +321,17 @@ int advance_device_step(fsdp_unit* u, cudaStream_t st) {
     return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "step-counter launch");
 }
 
-int enqueue_gather(fsdp_unit* u, uint16_t* out, cudaStream_t st) {
+// overlap: the stream's previous kernel is this step's first gather, which
+// writes the same bytes to `out` and touches nothing else this one does.
+int enqueue_gather(fsdp_unit* u, uint16_t* out, cudaStream_t st, bool overlap = false) {
     if (u->gather_source == FSDP_GATHER_FROM_SHADOW) {
         int rc = ensure_shadow(u, st);
         if (rc) return rc;
     }
     return profiled_launch(u, FSDP_KERNEL_GATHER, st, "gather launch", [&] {
         if (u->gather_source == FSDP_GATHER_FROM_SHADOW)
-            return fsdp::launch_gather_shadow(u->tiles, u->ntiles, u->shadow, out, st);
-        return fsdp::launch_gather(u->tiles, u->ntiles, u->master, out, st);
+            return fsdp::launch_gather_shadow(u->tiles, u->ntiles, u->shadow, out, st, overlap);
+        return fsdp::launch_gather(u->tiles, u->ntiles, u->master, out, st, overlap);
     });
 }
 
@@ -342,9 +344,13 @@ int check_rs_options(const fsdp_rs_options* opt) {
     return FSDP_OK;
 }
 
+// overlap: the stream's previous kernels are this step's gathers, which touch
+// neither the gradients nor the gradient shard (only the register-staged
+// kernels take it; the shared-memory staged ones wait at their start).
 int enqueue_reduce_scatter(fsdp_unit* u, const void* const* grads, int narrow, const fsdp_rs_options* opt,
-                           cudaStream_t st) {
+                           cudaStream_t st, bool overlap = false) {
     fsdp::ReduceArgs a{};
+    a.overlap = overlap ? 1 : 0;
     a.F = u->plan.N;
     a.groups = u->replicas;
     a.bf16_reduce = u->reduce_dtype == FSDP_DTYPE_BF16 ? 1 : 0;
@@ -714,10 +720,13 @@ int fsdp_step(fsdp_unit* u, const void* const* grads, uint16_t* out, const fsdp_
     DeviceGuard dg(u->device);
     if (!dg.ok()) return fail(FSDP_E_CUDA, "cannot select the unit's device");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the first gather waits for everything before it in the stream; the
+    // second gather and the reduce-scatter may start beside the kernel before
+    // them (each completes after it), and AdamW waits for all three
     rc = enqueue_gather(u, out, st);                       // forward
-    if (rc == FSDP_OK && u->raf) rc = enqueue_gather(u, out, st);   // backward re-gather
+    if (rc == FSDP_OK && u->raf) rc = enqueue_gather(u, out, st, true);   // backward re-gather
     if (rc == FSDP_OK && u->fuse) return enqueue_reduce_adamw(u, grads, narrow, hp, st);
-    if (rc == FSDP_OK) rc = enqueue_reduce_scatter(u, grads, narrow, nullptr, st);
+    if (rc == FSDP_OK) rc = enqueue_reduce_scatter(u, grads, narrow, nullptr, st, true);
     if (rc == FSDP_OK) rc = enqueue_adamw(u, hp, st);
     return rc;
 }

@@ -150,6 +150,24 @@ __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// The same for a kernel that touches nothing its predecessor writes or reads
+// (inside fsdp_step: the second gather after the first, the reduce-scatter
+// after the gathers).  With `overlap` it lets its successor be scheduled at
+// once and starts its work beside the predecessor's last wave, and waits for
+// the predecessor only before exiting (pdl_leave): it still completes after
+// it, so a kernel that waits on this one also finds every earlier one done.
+// Every block of the predecessor has already been scheduled when this grid
+// starts (it starts only once they have all released it), so the waiting
+// blocks cannot keep the predecessor from finishing.
+__device__ __forceinline__ void pdl_begin(bool overlap) {
+    if (!overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_leave(bool overlap) {
+    if (overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Correctly rounded (RNE) addition of two bf16 pairs.  It equals the fp32 sum
 // rounded once to bf16: the exact sum of two bf16 values rounded to fp32 and
 // then to bf16 cannot differ from it rounded straight to bf16, because fp32
@@ -208,8 +226,8 @@ __global__ void __launch_bounds__(kBlock) shard_in_kernel(const Tile* __restrict
 __global__ void __launch_bounds__(kBlock) gather_cast_kernel(const Tile* __restrict__ tiles,
                                                              int64_t ntiles,
                                                              const float* __restrict__ master,
-                                                             uint16_t* __restrict__ out) {
-    pdl_enter();
+                                                             uint16_t* __restrict__ out, int overlap) {
+    pdl_begin(overlap);
     const int tid = threadIdx.x;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const Tile tl = tiles[t];
@@ -234,6 +252,7 @@ __global__ void __launch_bounds__(kBlock) gather_cast_kernel(const Tile* __restr
             if (v < sp.nvec) st8bf(dst + 8 * v, pack8(r[u]));
         }
     }
+    pdl_leave(overlap);
 }
 
 // ---------------------------------------------------------------- gather from the shadow
@@ -241,8 +260,8 @@ __global__ void __launch_bounds__(kBlock) gather_cast_kernel(const Tile* __restr
 __global__ void __launch_bounds__(kBlock) gather_shadow_kernel(const Tile* __restrict__ tiles,
                                                                int64_t ntiles,
                                                                const uint16_t* __restrict__ shadow,
-                                                               uint16_t* __restrict__ out) {
-    pdl_enter();
+                                                               uint16_t* __restrict__ out, int overlap) {
+    pdl_begin(overlap);
     const int tid = threadIdx.x;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const Tile tl = tiles[t];
@@ -267,6 +286,7 @@ __global__ void __launch_bounds__(kBlock) gather_shadow_kernel(const Tile* __res
             if (v < sp.nvec) st8bf(dst + 8 * v, r[u]);
         }
     }
+    pdl_leave(overlap);
 }
 
 // ---------------------------------------------------------------- range cast
@@ -566,7 +586,7 @@ template <typename GT, int NMAX, bool BF16, bool EXT, bool NARROW>
 __global__ void __launch_bounds__(kBlock) reduce_scatter_kernel(const Tile* __restrict__ tiles,
                                                                 int64_t ntiles, GradPtrs<NMAX> gp,
                                                                 ReduceArgs a, float* __restrict__ gshard) {
-    pdl_enter();
+    pdl_begin(a.overlap != 0);
     const int tid = threadIdx.x;
     const int groups = EXT ? a.groups : 1;
     const float fW = static_cast<float>(a.F * groups);
@@ -617,6 +637,7 @@ __global__ void __launch_bounds__(kBlock) reduce_scatter_kernel(const Tile* __re
     if (found != nullptr) {   // uniform across the CTA
         if (__syncthreads_or(bad) && tid == 0) *found = 1;
     }
+    pdl_leave(a.overlap != 0);
 }
 
 // ---------------------------------------------------------------- AdamW
@@ -1280,15 +1301,18 @@ cudaError_t launch_shard_in(const Tile* tiles, int64_t ntiles, const ParamSrc* p
                       shadow);
 }
 
-cudaError_t launch_gather(const Tile* tiles, int64_t ntiles, const float* master, uint16_t* out, cudaStream_t st) {
+cudaError_t launch_gather(const Tile* tiles, int64_t ntiles, const float* master, uint16_t* out, cudaStream_t st,
+                          bool overlap) {
     if (ntiles == 0) return cudaSuccess;
-    return launch_pdl(gather_cast_kernel, grid_for(ntiles), kBlock, st, tiles, ntiles, master, out);
+    return launch_pdl(gather_cast_kernel, grid_for(ntiles), kBlock, st, tiles, ntiles, master, out,
+                      overlap ? 1 : 0);
 }
 
 cudaError_t launch_gather_shadow(const Tile* tiles, int64_t ntiles, const uint16_t* shadow,
-                                 uint16_t* out, cudaStream_t st) {
+                                 uint16_t* out, cudaStream_t st, bool overlap) {
     if (ntiles == 0) return cudaSuccess;
-    return launch_pdl(gather_shadow_kernel, grid_for(ntiles), kBlock, st, tiles, ntiles, shadow, out);
+    return launch_pdl(gather_shadow_kernel, grid_for(ntiles), kBlock, st, tiles, ntiles, shadow, out,
+                      overlap ? 1 : 0);
 }
 
 cudaError_t launch_cast_range(const float* master, uint16_t* shadow, int64_t begin, int64_t n, cudaStream_t st) {

@@ -47,6 +47,8 @@ struct ReduceArgs {
     int32_t* found;     // set to 1 when a written value is not finite; may be null
     int narrow;         // 1: some gradient buffer is only 16-byte aligned (16-byte loads)
     unsigned long long wait_ns;   // bound of each wait in the staged kernels (0: 10 s)
+    int overlap;        // register-staged kernels: may run beside the previous kernel
+                        // (touches nothing it touches; completes after it)
     int withhold;       // test of the give-up path: CTA 0 of a staged kernel arms its
                         // first stage's barrier but issues none of that stage's copies;
                         // 1: the drain skips that stage, 2: the drain waits for it too
@@ -56,13 +58,15 @@ struct ReduceArgs {
 cudaError_t launch_shard_in(const Tile* tiles, int64_t ntiles, const ParamSrc* params,
                             float* master, uint16_t* shadow, cudaStream_t st);
 
+// overlap: the kernel touches nothing the stream's previous kernel touches,
+// so it may run beside it (it still completes after it); see pdl_begin.
 cudaError_t launch_gather(const Tile* tiles, int64_t ntiles, const float* master,
-                          uint16_t* out, cudaStream_t st);
+                          uint16_t* out, cudaStream_t st, bool overlap = false);
 
 // The gather from the bf16 shadow shards (a copy; the cast was done by AdamW
 // or shard-in).
 cudaError_t launch_gather_shadow(const Tile* tiles, int64_t ntiles, const uint16_t* shadow,
-                                 uint16_t* out, cudaStream_t st);
+                                 uint16_t* out, cudaStream_t st, bool overlap = false);
 
 // grads: W = a.F * a.groups pointers (fp32 or bf16 per grad_dtype), each P elements.
 // kstatus: the unit's device status word (FSDP_KSTATUS_* bits).
