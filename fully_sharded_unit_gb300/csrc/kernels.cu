@@ -22,7 +22,10 @@
 // and starts with griddepcontrol.wait (pdl_enter), so the next kernel's CTAs
 // are scheduled during the previous kernel's last wave while the stream order
 // of every memory access stays the same (the staged fused kernel waits but
-// does not release its successor early).
+// does not release its successor early).  Inside a unit step the second
+// gather and the reduce-scatter, which share no memory with the kernel
+// before them, may instead start at once and wait only before exiting
+// (pdl_begin / pdl_leave with `overlap`).
 //
 // Numerics: every floating-point operation is an explicitly rounded
 // intrinsic (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so nothing is
