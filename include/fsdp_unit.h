@@ -357,7 +357,10 @@ FSDP_API int fsdp_reduce_scatter_flat_noalloc(const void* const* grads_dev, int 
  * bf16 for FSDP_STATE_SHADOW) to `dst`, or from `src` into the unit.  dst/src
  * may be device or host memory (cudaMemcpyAsync with cudaMemcpyDefault; use
  * pinned host memory for asynchrony).  Size = the rank's shard length.
- * Setting FSDP_STATE_PARAM also recomputes that rank's shadow as RNE(master). */
+ * Setting FSDP_STATE_PARAM also recomputes that rank's shadow as RNE(master).
+ * Reading (or setting) FSDP_STATE_SHADOW first enqueues, on `stream`, the
+ * recomputation of a shadow that AdamW left stale (see fsdp_adamw_step); so do
+ * fsdp_read_global and fsdp_read_arena. */
 FSDP_API int fsdp_get_state(const fsdp_unit* unit, int which, int rank, void* dst, void* stream);
 FSDP_API int fsdp_set_state(fsdp_unit* unit, int which, int rank, const void* src, void* stream);
 
