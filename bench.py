@@ -931,6 +931,7 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world,
 
     step()
     torch.cuda.synchronize()
+    link = host_link_rates(host_grads[0], grads[0], stream)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist_barrier(world)
     torch.cuda.synchronize()
@@ -949,7 +950,23 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world,
         del sets
     return {"value": world * step_bytes * args.e2e_steps / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "ms_per_step": ms / args.e2e_steps, "mode": mode, "inputs": inputs}
+            "ms_per_step": ms / args.e2e_steps, "mode": mode, "inputs": inputs, "host_link": link}
+
+
+def host_link_rates(host: torch.Tensor, dev: torch.Tensor, stream) -> dict:
+    """This machine's host link, measured just before the e2e timing: one copy of
+    `host` (pinned) to the device and one back, each alone (GB/s)."""
+    out = {}
+    for name, dst, src in (("h2d_gbs", dev, host), ("d2h_gbs", host, dev)):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        out[name] = src.numel() * src.element_size() / (ev0.elapsed_time(ev1) * 1e-3) / 1e9
+    return out
 
 
 def host_mem_available():
