@@ -315,7 +315,10 @@ def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None
     whose union is at least `frac` of the unit.  Every step's outputs
     (gathered bf16 parameters, gradient shards) and the final master, m, v and
     shadow are compared on the union of all of them.  ``cmp.covered`` is the
-    union's size; ``cmp.step_random`` each step's random coverage."""
+    union's size; ``cmp.step_random`` each step's random coverage.  For an
+    unfused unit, step 0 runs as the separate calls (gather, gather again,
+    reduce-scatter, AdamW) with the two gathers in two buffers, so both are
+    compared; later steps run through fsdp_step."""
     shapes = wl.shapes(unit)
     N, P = wl.N, wl.unit_numel(unit)
     steps = wl.steps if steps is None else steps
@@ -338,25 +341,40 @@ def run_windowed(wl: workloads.Workload, unit: int = 0, steps: int | None = None
         del params
         gdev = [torch.empty(P, dtype=wl.torch_grad_dtype(), device="cuda") for _ in range(wl.world)]
         out = torch.empty(P, dtype=torch.int16, device="cuda")
-        g_win, out_win, gs_win = [], [], []
+        # step 0 of an unfused unit runs as its separate calls with a buffer per
+        # gather, so that the first gather is compared too (fsdp_step writes
+        # both into one buffer); the other steps run through fsdp_step
+        split = not wl.fuse_reduce_adamw and steps > 1
+        first = torch.empty(P, dtype=torch.int16, device="cuda") if split else None
+        g_win, out_win, first_win, gs_win = [], [], [], []
         for s in range(steps):
             for r in range(wl.world):
                 workloads.grad_tensor(wl, unit, s, r, "cuda", out=gdev[r])
             g_win.append([grad_np(g[idx_dev]) for g in gdev])
-            u.step(gdev, out, hp)
-            torch.cuda.synchronize()
+            if split and s == 0:
+                u.allgather(first)
+                u.allgather(out) if wl.reshard_after_forward else out.copy_(first)
+                u.reduce_scatter(gdev)
+                u.adamw_step(hp)
+                torch.cuda.synchronize()
+                first_win.append(u16(first[idx_dev]))
+            else:
+                u.step(gdev, out, hp)
+                torch.cuda.synchronize()
             out_win.append(u16(out[idx_dev]))
             gs_win.append(np.concatenate([u.read_global("grad", a, b - a).cpu().numpy() for a, b in windows]))
         final = {w: np.concatenate([u.read_global(w, a, b - a).cpu().numpy() for a, b in windows])
                  for w in ("param", "exp_avg", "exp_avg_sq")}
         shadow = np.concatenate([u16(u.read_global("shadow", a, b - a)) for a, b in windows])
         assert u.kernel_status() == 0, "a kernel raised its status word"
-        del gdev, out, idx_dev
+        del gdev, out, idx_dev, first
     finally:
         u.close()
     kind = ("hybrid", N) if wl.replicas > 1 else ("bf16" if wl.reduce_dtype == "bf16" else "f32")
     per_step, (p, m, v), m_prev = oracle_windows(p_win, g_win, hp, kind)
     for s, (gathered, G) in enumerate(per_step):
+        if s < len(first_win):
+            assert_bits_equal(first_win[s], gathered, f"step {s} first gather (windows)")
         assert_bits_equal(out_win[s], gathered, f"step {s} gathered (windows)")
         assert_bits_equal(gs_win[s], G, f"step {s} grad shard (windows)")
     G_last = per_step[-1][1] if per_step else np.zeros_like(p)
