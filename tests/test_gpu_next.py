@@ -312,3 +312,53 @@ def test_switching_step_options_mid_run_changes_nothing():
     finally:
         a.close()
         b.close()
+
+
+def test_shadow_is_rne_of_master_whenever_read():
+    """AdamW stores the bf16 shadow only when the unit gathers from it; every
+    read of the shadow (state export, arena, a gather from it) must still see
+    RNE(master).  The hard case: the shadow is stale, the unit switches to the
+    shadow gather, and the next (shadow-storing) AdamW is skipped on the device
+    because its step table is used up; the library refreshes the shadow before
+    that launch, so it is right either way."""
+    wl = workloads.get("ragged_mini_flat_n7")
+    hp = workloads.hyper(wl)
+    u = B.Unit(wl.shapes(0), wl.layout, wl.N)                 # gathers from the fp32 master
+    try:
+        u.load([p.cuda() for p in workloads.param_tensors(wl, 0)])
+        grads = [workloads.grad_tensor(wl, 0, 0, r).cuda() for r in range(wl.N)]
+        out = torch.empty(u.numel, dtype=torch.int16, device="cuda")
+
+        def check(what):
+            torch.cuda.synchronize()
+            master = u.read_global("param").cpu().numpy()
+            H.assert_bits_equal(H.u16(u.read_global("shadow")), O.bf16_rne(master), what)
+            for k in range(u.N):
+                H.assert_bits_equal(H.u16(u.get_state("shadow", k)),
+                                    O.bf16_rne(u.get_state("param", k).cpu().numpy()), f"{what} rank {k}")
+
+        u.step(grads, out, hp)                                 # AdamW leaves the shadow stale
+        check("after a master-gather step")
+        u.step(grads, out, hp)
+        B.fsdp_adamw_device_steps(u.handle, hp, 1)
+        u.adamw_step(hp)                                       # uses the table's only step, no shadow store
+        B.fsdp_unit_set_step_options(u.handle, "shadow", False)
+        u.adamw_step(hp)                                       # shadow-storing, skipped: table used up
+        assert B.fsdp_adamw_device_status(u.handle)[1]
+        check("after a skipped shadow-storing step")
+        B.fsdp_adamw_device_steps(u.handle, None, 0)
+        u.step(grads, out, hp)                                 # gathers from the shadow
+        torch.cuda.synchronize()
+        # the gathered buffer is RNE of the master before this step's AdamW:
+        # compare against a fresh master-gather of the same state instead
+        B.fsdp_unit_set_step_options(u.handle, "master", False)
+        ref = torch.empty_like(out)
+        u.allgather(ref)
+        B.fsdp_unit_set_step_options(u.handle, "shadow", False)
+        got = torch.empty_like(out)
+        u.allgather(got)
+        torch.cuda.synchronize()
+        assert torch.equal(ref, got)
+        check("after a shadow-gather step")
+    finally:
+        u.close()
