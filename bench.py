@@ -586,7 +586,7 @@ def run_ours(args, world, rank, local):
         # the host link's speed differs from box to box, and so does which way
         # of moving the gradients in is faster: "auto" times both and reports
         # the faster, with both figures
-        modes = ["pipelined", "zero_copy"] if args.e2e_mode == "auto" else [args.e2e_mode]
+        modes = ["pipelined", "pipelined_direct", "zero_copy"] if args.e2e_mode == "auto" else [args.e2e_mode]
         runs = [run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world, m) for m in modes]
         timed = [r for r in runs if r.get("value") is not None]
         e2e = min(timed, key=lambda r: r["ms_per_step"]) if timed else runs[0]
@@ -831,7 +831,11 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world,
                    computes (the first unit of the next step while this step's
                    last unit computes); the reduce-scatter waits for its unit's
                    copies.  Every timed step's copies start after the timed
-                   region opens.
+                   region opens;
+      pipelined_direct -- pipelined, but the first gather's kernel stores the
+                   gathered parameters straight into the pinned host buffer
+                   (a device address from fsdp_host_device_pointer), so no
+                   device->host copy runs beside the host->device ones.
     The unit step is issued as its calls (gather, gather again, reduce-scatter,
     AdamW: the work of fsdp_step) so that the gathered parameters, final after
     the first gather, are copied to the host on a second stream while the rest
@@ -863,6 +867,10 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world,
     outs = [(out, torch.empty_like(out)), (torch.empty_like(out), torch.empty_like(out))]
     copy_stream = torch.cuda.Stream(device=dev)
     h2d_stream = torch.cuda.Stream(device=dev)
+    direct = mode == "pipelined_direct"   # the first gather writes straight into pinned host memory
+    if direct:
+        mode = "pipelined"
+        host_out_dev = [B.fsdp_host_device_pointer(h) for h in host_out]
     if mode == "zero_copy":
         unit_grads = [[B.fsdp_host_device_pointer(h[:u.numel]) for h in host_grads] for u in units]
     elif mode == "pipelined":
@@ -904,16 +912,20 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world,
             if mode == "copy":
                 for h, g in zip(host_grads, grads):
                     g[:u.numel].copy_(h[:u.numel], non_blocking=True)
-            u.allgather(first[:u.numel], stream)
-            ready = torch.cuda.Event()
-            ready.record(stream)
-            copy_stream.wait_event(ready)
-            with torch.cuda.stream(copy_stream):
-                host_out[i][:u.numel].copy_(first[:u.numel], non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(copy_stream)
-            free[i % 2] = ev
-            done.append(ev)
+            if direct:   # gathered parameters stored over the host link by the kernel itself
+                rc = B.lib().fsdp_allgather(u.handle, host_out_dev[i].data_ptr(), stream.cuda_stream)
+                assert rc == B.FSDP_OK, B.fsdp_last_error()
+            else:
+                u.allgather(first[:u.numel], stream)
+                ready = torch.cuda.Event()
+                ready.record(stream)
+                copy_stream.wait_event(ready)
+                with torch.cuda.stream(copy_stream):
+                    host_out[i][:u.numel].copy_(first[:u.numel], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy_stream)
+                free[i % 2] = ev
+                done.append(ev)
             if wl.reshard_after_forward:
                 u.allgather(second[:u.numel], stream)
             if mode == "pipelined":
@@ -950,7 +962,8 @@ def run_e2e(args, wl, units, grads, out, hp, cb, step_bytes, stream, dev, world,
         del sets
     return {"value": world * step_bytes * args.e2e_steps / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "ms_per_step": ms / args.e2e_steps, "mode": mode, "inputs": inputs, "host_link": link}
+            "ms_per_step": ms / args.e2e_steps, "mode": "pipelined_direct" if direct else mode, "inputs": inputs,
+            "host_link": link}
 
 
 def host_link_rates(host: torch.Tensor, dev: torch.Tensor, stream) -> dict:
@@ -989,11 +1002,14 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mingpt175b_flat", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--e2e-mode", choices=["auto", "pipelined", "zero_copy", "copy"], default="auto",
+    ap.add_argument("--e2e-mode", choices=["auto", "pipelined", "pipelined_direct", "zero_copy", "copy"],
+                    default="auto",
                     help="pipelined: gradients copied host->device on their own stream into two "
                          "alternating device sets while the previous unit computes; zero_copy: the "
-                         "reduce-scatter reads pinned host memory directly; copy: copies on the "
-                         "compute stream; auto: time pipelined and zero_copy, report the faster")
+                         "reduce-scatter reads pinned host memory directly; pipelined_direct: "
+                         "pipelined, with the first gather writing straight into pinned host "
+                         "memory (no device->host copy); copy: copies on the compute stream; "
+                         "auto: time pipelined, pipelined_direct and zero_copy, report the fastest")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
